@@ -1,0 +1,209 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4.so, a GB300 (sm_103a) NVFP4
+ * routed-expert MoE layer step.
+ *
+ * The step, as stated on the rocket blog page "The CUTLASS grouped GEMM beats
+ * the scalar GEMV loop at every M, M=1 included" (section "What changed"):
+ *   gather -> quantize (NVFP4) -> grouped GEMM w13 (fused gate|up, alpha = 1)
+ *   -> SwiGLU with per-group gate/up weight_scale_2 -> quantize -> grouped
+ *   GEMM w2 -> scatter-add weighted by router weight * down weight_scale_2.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless a comment says
+ *     "host". The library allocates no device memory.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Work is enqueued on `stream` and runs asynchronously; nothing here
+ *     synchronizes except moe_nvfp4_check_status.
+ *   - Return value: MOE_OK, or an error code. Arguments are validated on the
+ *     host before anything is enqueued; an error return enqueues nothing,
+ *     except MOE_ERR_CUDA (a launch failed part way).
+ *   - Results are deterministic: the same inputs give bit-identical outputs,
+ *     and a token's output does not depend on which other tokens share the
+ *     batch (fixed expert order, no atomics in any reduction).
+ *
+ * NVFP4 formats (page "Fusing the MoE layer's two grouped GEMMs is worth 4%",
+ * table "Bytes decide it before the kernel runs": 0.5 + 1/16 byte/element)
+ *   - packed e2m1: two 4-bit codes per byte, element 2j in bits 0-3 of byte
+ *     j, element 2j+1 in bits 4-7; code bit 3 is the sign, magnitudes
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   - block scales: one e4m3 (E4M3FN) byte per 16 consecutive elements of a
+ *     row, stored in 128-row atoms (the tcgen05 / CUTLASS SFA-SFB layout the
+ *     first page's section "The seam CUTLASS forced open" names). With
+ *     Kc = K/16 scale columns, scale (row m, column c) of a region sits at
+ *       ((m/128)*(Kc/4) + c/4)*512 + (m%32)*16 + ((m/32)%4)*4 + (c%4).
+ *   - activations carry no global scale (alpha = 1): block scale =
+ *     e4m3_rne_satfinite(amax/6); codes = e2m1_rne_satfinite(x/scale); both
+ *     divisions correctly rounded fp32; a block whose scale is 0 has all-zero
+ *     codes.
+ *   - weights carry one fp32 global per projection (weight_scale_2); gate and
+ *     up have their own (second page, "Different globals on the two halves").
+ *
+ * Routing: topk_ids[T, k] int32, topk_w[T, k] fp32. Slot s = t*k + j. An id
+ * outside [0, E) marks an unused slot (it adds nothing to its token). Rows are
+ * grouped by ascending expert id and, inside a group, by ascending slot
+ * (first page, "What changed": ordered map, batch-invariant group order).
+ * Activation scale regions are laid out per group, each padded with zero bytes
+ * to a multiple of 128 rows; packed rows are contiguous with no padding.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,   /* null pointer, negative size, k > 32, E > 1024, ... */
+  MOE_ERR_SHAPE = 2,     /* unsupported shape: a K not multiple of 64, an N not multiple of 128 */
+  MOE_ERR_CUDA = 3,      /* a CUDA call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 4,   /* a device-side wait gave up (reported by moe_nvfp4_check_status) */
+  MOE_ERR_WORKSPACE = 5  /* workspace smaller than moe_nvfp4_layer_workspace_size() */
+};
+
+/* Group metadata produced by moe_route_groups (device int32 arrays, caller
+ * owned; moe_groups_carve lays them out in one buffer).
+ *   counts[4]            G (groups), R (rows), max Mg, total 128-row scale blocks
+ *   group_offsets[E+1]   first row of group g; entry G holds R
+ *   group_expert[E]      expert id of group g (ascending)
+ *   group_sf_block[E+1]  first 128-row scale block of group g; entry G = total
+ *   row_slot[T*k]        slot t*k+j of grouped row r (r < R)
+ *   slot_row[T*k]        grouped row of slot s, or -1 for an unused slot     */
+typedef struct {
+  int32_t* counts;
+  int32_t* group_offsets;
+  int32_t* group_expert;
+  int32_t* group_sf_block;
+  int32_t* row_slot;
+  int32_t* slot_row;
+} moe_groups_t;
+
+/* Expert weights (device). w13 rows 0..I-1 are gate, I..2I-1 are up, back to
+ * back; w13_sf is gate's atom region followed by up's (first page, "The seam
+ * CUTLASS forced open"; bit-identical to one region over 2I rows because
+ * I % 128 == 0). */
+typedef struct {
+  int E;
+  const uint8_t* w13_packed;  /* [E, 2I, H/2] */
+  const uint8_t* w13_sf;      /* [E, 2I*H/16] atom layout, one region per expert */
+  const float* g_gate_up;     /* [E, 2]: gate global, up global */
+  const uint8_t* w2_packed;   /* [E, H, I/2] */
+  const uint8_t* w2_sf;       /* [E, H*I/16] atom layout */
+  const float* g_down;        /* [E] */
+} moe_nvfp4_weights_t;
+
+/* Message for a status code (static string; never NULL). */
+const char* moe_nvfp4_error_string(int status);
+
+/* Reads and clears the device-side status word of the current device after
+ * synchronizing `stream`: MOE_OK, or MOE_ERR_TIMEOUT if a kernel's bounded
+ * wait gave up since the last check (its outputs are then invalid). Returns
+ * MOE_ERR_CUDA if the synchronization itself fails. */
+int moe_nvfp4_check_status(cudaStream_t stream);
+
+/* Bytes of the group metadata for T tokens, top-k, E experts; and a carve of
+ * one caller buffer `mem` (256-byte aligned, that many bytes) into
+ * moe_groups_t (host struct filled in; no device work). */
+size_t moe_groups_bytes(int T, int k, int E);
+int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* groups /* host */);
+
+/* Bytes of a per-group padded scale region able to hold any grouping of up to
+ * R_max rows over E experts for a K-wide operand:
+ * (min(E, R_max) + ceil(R_max/128)) * 128 * K/16. */
+size_t nvfp4_sf_bytes(int R_max, int E, int K);
+
+/* a1 -- route-group. Counts the T*k slots per expert, scans, and places rows
+ * stably by (expert ascending, slot ascending); fills *groups on the device.
+ * First page, "What changed" (std::map grouping, one fetch per expert) and
+ * "Next" (host grouping cost). One CTA; E <= 1024. */
+int moe_route_groups(const int32_t* topk_ids, int T, int k, int E,
+                     const moe_groups_t* groups /* host struct of device pointers */,
+                     cudaStream_t stream);
+
+/* a1 + a2 -- moe_gather_rows: groups the slots (as moe_route_groups) and
+ * copies x[slot/k, :] into grouped row order. xg [T*k, H] bf16; rows >= R
+ * are left untouched. First page, "What changed": normed_[stream] -> one row
+ * per (stream, expert). */
+int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, int k, int E,
+                    const moe_groups_t* groups, uint16_t* xg, cudaStream_t stream);
+
+/* a3 / a6 -- nvfp4_quantize_rows: grouped bf16 rows [R_max, K] -> packed
+ * [R_max, K/2] (rows >= R untouched) and the per-group padded scale region
+ * `sf` (nvfp4_sf_bytes(R_max, E, K) bytes; padding bytes written as 0).
+ * First page, "What changed" and "Proof" (byte-for-byte vs the host codec,
+ * group_m = {1, 130}). K % 64 == 0. */
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, const moe_groups_t* groups,
+                        uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+
+/* a2 + a3 fused: quantizes x[row_slot[r]/k, :] straight into grouped NVFP4
+ * rows; output identical to moe_gather_rows followed by nvfp4_quantize_rows. */
+int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, const moe_groups_t* groups,
+                             uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+
+/* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
+ * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
+ * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
+ * W is [E, N, K/2] packed with w_sf [E, N*K/16] in the atom layout. One
+ * launch for all groups on tcgen05 block-scaled MMA (kind::mxf4nvf4, scale
+ * vector 16), accumulators in tensor memory. First page, "What changed":
+ * grouped GEMM w13 N=4096 K=4096 and w2 N=4096 K=2048, alpha = 1.
+ * N % 128 == 0, K % 64 == 0. */
+int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
+                       int R_max, const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K,
+                       float* d, cudaStream_t stream);
+
+/* a5 -- swiglu_grouped: h[r, n] = silu(d13[r, n]*g_gate[e]) * (d13[r, I+n]*g_up[e]),
+ * computed in fp32 (CUDA expf) and rounded once to bf16. d13 [R_max, 2I]
+ * fp32, h [R_max, I] bf16. Second page, "Different globals on the two halves",
+ * option (a): the per-half globals are applied here. */
+int swiglu_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups,
+                   const float* g_gate_up, uint16_t* h, cudaStream_t stream);
+
+/* a5 + a6 fused: SwiGLU as swiglu_grouped, then the a3 codec on the bf16 h,
+ * written as packed [R_max, I/2] + per-group padded scales
+ * (nvfp4_sf_bytes(R_max, E, I) bytes). Identical to swiglu_grouped followed
+ * by nvfp4_quantize_rows. */
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups,
+                            const float* g_gate_up, uint8_t* packed, uint8_t* sf,
+                            cudaStream_t stream);
+
+/* a8 -- moe_scatter_add: y[t, :] = sum over t's used slots, in ascending
+ * grouped-row order (= ascending expert id), of topk_w[t, j] * g_down[e] *
+ * d2[row, :]; fp32 accumulation, rounded once to bf16. y [T, H] is
+ * overwritten; a token with no used slot gets zeros. First page, "What
+ * changed" (weighted by router weight * down weight_scale_2) and "Proof"
+ * (shared accumulator row, ordered accumulation). k <= 32. */
+int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w,
+                    int T, int k, int E, const moe_groups_t* groups, const float* g_down,
+                    uint16_t* y, cudaStream_t stream);
+
+/* Workspace bytes of moe_nvfp4_layer for these sizes (group metadata, NVFP4
+ * activations and scales, fp32 GEMM outputs). */
+size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I);
+
+/* The whole step a1..a8 on `stream`: route-group, gather+quantize, grouped
+ * GEMM w13, SwiGLU+requantize, grouped GEMM w2, scatter-add. x [T, H] bf16,
+ * y [T, H] bf16 (overwritten). `workspace` is caller device memory of
+ * ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I), 256-byte
+ * aligned. H % 128 == 0, I % 128 == 0, k <= 32, E <= 1024. */
+int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
+                    const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
+                    void* workspace, size_t ws_bytes, uint16_t* y, cudaStream_t stream);
+
+/* Load-time helper (not part of the timed step): linear row-major scales
+ * [N, K/16] -> the atom layout, N padded up to a multiple of 128 with zero
+ * bytes (output ceil(N/128)*128*K/16 bytes). First page, "The seam CUTLASS
+ * forced open": fuel::swizzle_block_scales, once per projection.
+ * K % 64 == 0. */
+int nvfp4_swizzle_block_scales(const uint8_t* linear, int N, int K, uint8_t* swizzled,
+                               cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,258 @@
+"""ctypes binding of libmoe_nvfp4.so (include/moe_nvfp4.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (device memory and streams only); calls are
+enqueued on the current torch stream. A nonzero status raises RuntimeError.
+There is no fallback: if the library cannot be built or loaded, load()
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+_LIB = None
+
+c_int, c_size_t, c_void_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+
+class MoeGroups(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("counts", "group_offsets", "group_expert", "group_sf_block",
+                                       "row_slot", "slot_row")]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("E", c_int), ("w13_packed", c_void_p), ("w13_sf", c_void_p), ("g_gate_up", c_void_p),
+                ("w2_packed", c_void_p), ("w2_sf", c_void_p), ("g_down", c_void_p)]
+
+
+_SIGS = {
+    "moe_nvfp4_error_string": (ctypes.c_char_p, [c_int]),
+    "moe_nvfp4_check_status": (c_int, [c_void_p]),
+    "moe_groups_bytes": (c_size_t, [c_int, c_int, c_int]),
+    "moe_groups_carve": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups)]),
+    "nvfp4_sf_bytes": (c_size_t, [c_int, c_int, c_int]),
+    "moe_route_groups": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p]),
+    "moe_gather_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups),
+                                c_void_p, c_void_p]),
+    "nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
+                                    c_void_p]),
+    "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
+                                         c_void_p, c_void_p]),
+    "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_void_p,
+                                   c_int, c_int, c_int, c_void_p, c_void_p]),
+    "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
+                               c_void_p]),
+    "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
+                                        c_void_p, c_void_p, c_void_p]),
+    "moe_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                                ctypes.POINTER(MoeGroups), c_void_p, c_void_p, c_void_p]),
+    "moe_nvfp4_layer_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "moe_nvfp4_layer": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
+                                ctypes.POINTER(MoeWeights), c_void_p, c_size_t, c_void_p, c_void_p]),
+    "nvfp4_swizzle_block_scales": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
+}
+
+
+def load():
+    """Builds (if stale) and loads the library; raises if either fails."""
+    global _LIB
+    if _LIB is None:
+        path = _build.ensure_built()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = lib
+    return _LIB
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name, status):
+    if status != 0:
+        msg = load().moe_nvfp4_error_string(status).decode()
+        raise RuntimeError(f"{name} failed: {msg} (status {status})")
+
+
+class Groups:
+    """Device buffer holding the group metadata of T tokens, top-k, E experts,
+    with torch views of its arrays for inspection."""
+
+    def __init__(self, T: int, k: int, E: int, device="cuda"):
+        import torch
+        lib = load()
+        self.T, self.k, self.E = T, k, E
+        nbytes = lib.moe_groups_bytes(T, k, E)
+        self.buffer = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        self.struct = MoeGroups()
+        _check("moe_groups_carve", lib.moe_groups_carve(_ptr(self.buffer), T, k, E, ctypes.byref(self.struct)))
+
+    def view(self, name: str, n: int):
+        import torch
+        off = getattr(self.struct, name) - self.buffer.data_ptr()
+        return self.buffer[off:off + 4 * n].view(torch.int32)
+
+    def host(self) -> dict:
+        """Copies the metadata to the host (synchronizes)."""
+        counts = self.view("counts", 4).cpu()
+        G, R, maxmg, nblk = (int(v) for v in counts)
+        S = self.T * self.k
+        return dict(G=G, R=R, max_mg=maxmg, blocks=nblk,
+                    group_offsets=self.view("group_offsets", G + 1).cpu(),
+                    group_expert=self.view("group_expert", G).cpu(),
+                    group_sf_block=self.view("group_sf_block", G + 1).cpu(),
+                    row_slot=self.view("row_slot", R).cpu(),
+                    slot_row=self.view("slot_row", S).cpu())
+
+
+def sf_bytes(R_max: int, E: int, K: int) -> int:
+    return load().nvfp4_sf_bytes(R_max, E, K)
+
+
+def check_status(stream=None) -> int:
+    return load().moe_nvfp4_check_status(_stream(stream))
+
+
+def moe_route_groups(topk_ids, E: int, groups: Groups, stream=None):
+    T, k = topk_ids.shape
+    _check("moe_route_groups", load().moe_route_groups(_ptr(topk_ids), T, k, E, ctypes.byref(groups.struct),
+                                                       _stream(stream)))
+
+
+def moe_gather_rows(x, topk_ids, E: int, groups: Groups, xg, stream=None):
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_gather_rows", load().moe_gather_rows(_ptr(x), T, H, _ptr(topk_ids), k, E,
+                                                     ctypes.byref(groups.struct), _ptr(xg), _stream(stream)))
+
+
+def nvfp4_quantize_rows(rows, groups: Groups, packed, sf, stream=None):
+    R, K = rows.shape
+    _check("nvfp4_quantize_rows", load().nvfp4_quantize_rows(_ptr(rows), R, K, ctypes.byref(groups.struct),
+                                                             _ptr(packed), _ptr(sf), _stream(stream)))
+
+
+def moe_gather_quantize_rows(x, k: int, groups: Groups, packed, sf, stream=None):
+    T, H = x.shape
+    _check("moe_gather_quantize_rows",
+           load().moe_gather_quantize_rows(_ptr(x), T, H, k, ctypes.byref(groups.struct), _ptr(packed), _ptr(sf),
+                                           _stream(stream)))
+
+
+def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w_packed, w_sf, d, stream=None):
+    R_max = a_packed.shape[0]
+    K = a_packed.shape[1] * 2
+    E, N = w_packed.shape[0], w_packed.shape[1]
+    _check("nvfp4_grouped_gemm",
+           load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max,
+                                     _ptr(w_packed), _ptr(w_sf), E, N, K, _ptr(d), _stream(stream)))
+
+
+def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):
+    R_max, I2 = d13.shape
+    _check("swiglu_grouped", load().swiglu_grouped(_ptr(d13), R_max, I2 // 2, ctypes.byref(groups.struct),
+                                                   _ptr(g_gate_up), _ptr(h), _stream(stream)))
+
+
+def swiglu_quantize_grouped(d13, groups: Groups, g_gate_up, packed, sf, stream=None):
+    R_max, I2 = d13.shape
+    _check("swiglu_quantize_grouped",
+           load().swiglu_quantize_grouped(_ptr(d13), R_max, I2 // 2, ctypes.byref(groups.struct), _ptr(g_gate_up),
+                                          _ptr(packed), _ptr(sf), _stream(stream)))
+
+
+def moe_scatter_add(d2, topk_ids, topk_w, E: int, groups: Groups, g_down, y, stream=None):
+    T, k = topk_ids.shape
+    H = y.shape[1]
+    _check("moe_scatter_add",
+           load().moe_scatter_add(_ptr(d2), H, _ptr(topk_ids), _ptr(topk_w), T, k, E, ctypes.byref(groups.struct),
+                                  _ptr(g_down), _ptr(y), _stream(stream)))
+
+
+def nvfp4_swizzle_block_scales(linear, swizzled, stream=None):
+    """linear [N, K/16] u8 -> swizzled (ceil(N/128)*128*K/16 bytes)."""
+    N, Kc = linear.shape
+    _check("nvfp4_swizzle_block_scales",
+           load().nvfp4_swizzle_block_scales(_ptr(linear), N, Kc * 16, _ptr(swizzled), _stream(stream)))
+
+
+def moe_nvfp4_layer_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int:
+    return load().moe_nvfp4_layer_workspace_size(T, k, E, H, I)
+
+
+class Weights:
+    """Device NVFP4 expert weights in the layout moe_nvfp4_layer reads.
+
+    Built from packed nibbles, LINEAR block scales and globals; the scales are
+    swizzled into the atom layout once here (load time, on the GPU)."""
+
+    def __init__(self, w13_packed, w13_sf_linear, g_gate_up, w2_packed, w2_sf_linear, g_down, stream=None):
+        import torch
+        self.E, I2, H2 = w13_packed.shape
+        self.H, self.I = H2 * 2, I2 // 2
+        self.w13_packed = w13_packed.contiguous()
+        self.w2_packed = w2_packed.contiguous()
+        self.g_gate_up = g_gate_up.to(torch.float32).contiguous()
+        self.g_down = g_down.to(torch.float32).contiguous()
+        dev = w13_packed.device
+        self.w13_sf = torch.empty((self.E, 2 * self.I * self.H // 16), dtype=torch.uint8, device=dev)
+        self.w2_sf = torch.empty((self.E, self.H * self.I // 16), dtype=torch.uint8, device=dev)
+        nvfp4_swizzle_block_scales(w13_sf_linear.reshape(-1, self.H // 16).contiguous(), self.w13_sf, stream)
+        nvfp4_swizzle_block_scales(w2_sf_linear.reshape(-1, self.I // 16).contiguous(), self.w2_sf, stream)
+        self.struct = MoeWeights(self.E, self.w13_packed.data_ptr(), self.w13_sf.data_ptr(),
+                                 self.g_gate_up.data_ptr(), self.w2_packed.data_ptr(), self.w2_sf.data_ptr(),
+                                 self.g_down.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.w13_packed, self.w13_sf, self.w2_packed, self.w2_sf))
+
+
+def moe_nvfp4_layer(x, topk_ids, topk_w, weights: Weights, workspace, y, stream=None):
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_nvfp4_layer",
+           load().moe_nvfp4_layer(_ptr(x), T, H, weights.I, _ptr(topk_ids), _ptr(topk_w), k,
+                                  ctypes.byref(weights.struct), _ptr(workspace), workspace.numel(), _ptr(y),
+                                  _stream(stream)))
+
+
+class MoeLayer:
+    """Holds the weights and a workspace sized for up to T_max tokens."""
+
+    def __init__(self, weights: Weights, T_max: int, k: int):
+        import torch
+        self.weights, self.k, self.T_max = weights, k, T_max
+        n = moe_nvfp4_layer_workspace_size(T_max, k, weights.E, weights.H, weights.I)
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=weights.w13_packed.device)
+
+    def __call__(self, x, topk_ids, topk_w, y=None, stream=None):
+        import torch
+        assert x.shape[0] <= self.T_max and topk_ids.shape[1] == self.k
+        if y is None:
+            y = torch.empty_like(x)
+        moe_nvfp4_layer(x, topk_ids, topk_w, self.weights, self.workspace, y, stream)
+        return y

@@ -1,0 +1,46 @@
+// Host-side launchers shared by the translation units of libmoe_nvfp4.so.
+// Each returns cudaSuccess or the launch error; arguments are validated by
+// the C-ABI layer (moe_api.cu) before these are called.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/moe_nvfp4.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Upper bound on 128-row scale blocks for R_max rows in at most G_max groups.
+inline long long sf_blocks_bound(long long R_max, long long G_max) {
+  long long g = G_max < R_max ? G_max : R_max;
+  return g + (R_max + 127) / 128;
+}
+
+int num_sms();  // SM count of the current device (cached per device)
+
+cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g,
+                         cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g,
+                          uint16_t* xg, cudaStream_t s);
+// src_k > 0: rows are x[row_slot[r] / src_k]; src_k == 0: rows are src[r].
+cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int K,
+                            const moe_groups_t& g, uint8_t* packed, uint8_t* sf, cudaStream_t s);
+// h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
+cudaError_t launch_swiglu(const float* d13, int R_max, int I, const moe_groups_t& g,
+                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf,
+                          cudaStream_t s);
+cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w,
+                           int T, int k, int E, const moe_groups_t& g, const float* g_down,
+                           uint16_t* y, cudaStream_t s);
+cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s);
+
+// tcgen05 grouped GEMM (nvfp4_gemm.cu). status: device word for wait timeouts.
+cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf,
+                                const moe_groups_t& g, int R_max, const uint8_t* w_packed,
+                                const uint8_t* w_sf, int E, int N, int K, float* d, int* status,
+                                cudaStream_t s);
+
+}  // namespace moe

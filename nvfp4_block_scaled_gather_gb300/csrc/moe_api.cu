@@ -1,0 +1,271 @@
+// C ABI of libmoe_nvfp4.so: argument checks, workspace carving and the fused
+// layer entry. The kernels live in moe_kernels.cu and nvfp4_gemm.cu.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+
+// Device-side status word: kernels whose bounded waits expire write
+// MOE_ERR_TIMEOUT here; moe_nvfp4_check_status reads and clears it.
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices] = {0};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Device address of g_status_word on the current device (set up once per device).
+int* status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool groups_ok(const moe_groups_t* g) {
+  return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->row_slot && g->slot_row;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct LayerWs {
+  moe_groups_t groups;
+  uint8_t *xq, *xsf, *hq, *hsf;
+  float *d13, *d2;
+  size_t bytes;
+};
+
+// Carves the layer workspace; base may be null to only compute the size.
+LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
+  LayerWs w;
+  const size_t S = (size_t)T * k;
+  const long long nblk = sf_blocks_bound((long long)S, E);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  uint8_t* gmem = take(moe_groups_bytes(T, k, E));
+  if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
+  w.xq = take(S * H / 2);
+  w.xsf = take((size_t)nblk * 128 * (H / 16));
+  w.d13 = reinterpret_cast<float*>(take(S * 2 * I * sizeof(float)));
+  w.hq = take(S * I / 2);
+  w.hsf = take((size_t)nblk * 128 * (I / 16));
+  w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 148;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_nvfp4_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int moe_nvfp4_check_status(cudaStream_t stream) {
+  int* p = status_ptr();
+  if (!p) return MOE_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, p, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return host;
+}
+
+size_t moe_groups_bytes(int T, int k, int E) {
+  if (T < 0 || k < 0 || E < 0) return 0;
+  const size_t S = (size_t)T * k;
+  return align256(16 * 4) + align256(4 * (size_t)(E + 1)) + align256(4 * (size_t)E) +
+         align256(4 * (size_t)(E + 1)) + 2 * align256(4 * S);
+}
+
+int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
+  if (!mem || !g || T < 0 || k < 0 || E <= 0) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(mem) % 256) return MOE_ERR_INVALID;
+  const size_t S = (size_t)T * k;
+  uint8_t* p = static_cast<uint8_t*>(mem);
+  g->counts = reinterpret_cast<int32_t*>(p); p += align256(16 * 4);
+  g->group_offsets = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
+  g->group_expert = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)E);
+  g->group_sf_block = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
+  g->row_slot = reinterpret_cast<int32_t*>(p); p += align256(4 * S);
+  g->slot_row = reinterpret_cast<int32_t*>(p);
+  return MOE_OK;
+}
+
+size_t nvfp4_sf_bytes(int R_max, int E, int K) {
+  if (R_max < 0 || E < 0 || K < 0) return 0;
+  return (size_t)sf_blocks_bound(R_max, E) * 128 * (K / 16);
+}
+
+int moe_route_groups(const int32_t* topk_ids, int T, int k, int E, const moe_groups_t* groups, cudaStream_t stream) {
+  if (!groups_ok(groups) || T < 0 || k < 0 || E <= 0) return MOE_ERR_INVALID;
+  if (E > kMaxExperts || k > kMaxTopK) return MOE_ERR_INVALID;
+  if ((long long)T * k > (1LL << 30)) return MOE_ERR_INVALID;
+  if ((long long)T * k > 0 && !topk_ids) return MOE_ERR_INVALID;
+  return status_of(launch_route(topk_ids, T * k, E, *groups, stream));
+}
+
+int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, int k, int E,
+                    const moe_groups_t* groups, uint16_t* xg, cudaStream_t stream) {
+  if (H <= 0 || H % 8 || (T > 0 && k > 0 && (!x || !xg))) return MOE_ERR_INVALID;
+  const int st = moe_route_groups(topk_ids, T, k, E, groups, stream);
+  if (st != MOE_OK || T * k == 0) return st;
+  return status_of(launch_gather(x, H, k, T * k, *groups, xg, stream));
+}
+
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, const moe_groups_t* groups, uint8_t* packed,
+                        uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || K <= 0) return MOE_ERR_INVALID;
+  if (K % 64) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!rows || !packed || !sf) return MOE_ERR_INVALID;
+  return status_of(launch_quantize(rows, 0, R_max, K, *groups, packed, sf, stream));
+}
+
+int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, const moe_groups_t* groups, uint8_t* packed,
+                             uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0) return MOE_ERR_INVALID;
+  if (H % 64) return MOE_ERR_SHAPE;
+  if (T * k == 0) return MOE_OK;
+  if (!x || !packed || !sf) return MOE_ERR_INVALID;
+  return status_of(launch_quantize(x, k, T * k, H, *groups, packed, sf, stream));
+}
+
+int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
+                       const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K, float* d,
+                       cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID;
+  if (N % 128 || K % 64) return MOE_ERR_SHAPE;
+  if ((long long)E * N > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!a_packed || !a_sf || !w_packed || !w_sf || !d) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(a_packed) % 16 || reinterpret_cast<uintptr_t>(w_packed) % 16 ||
+      reinterpret_cast<uintptr_t>(a_sf) % 16 || reinterpret_cast<uintptr_t>(w_sf) % 16)
+    return MOE_ERR_INVALID;
+  int* st = status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_packed, w_sf, E, N, K, d, st, stream));
+}
+
+int swiglu_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups, const float* g_gate_up,
+                   uint16_t* h, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || I <= 0) return MOE_ERR_INVALID;
+  if (I % 64) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
+  return status_of(launch_swiglu(d13, R_max, I, *groups, g_gate_up, h, nullptr, nullptr, stream));
+}
+
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups, const float* g_gate_up,
+                            uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || I <= 0) return MOE_ERR_INVALID;
+  if (I % 64) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
+  return status_of(launch_swiglu(d13, R_max, I, *groups, g_gate_up, nullptr, packed, sf, stream));
+}
+
+int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k, int E,
+                    const moe_groups_t* groups, const float* g_down, uint16_t* y, cudaStream_t stream) {
+  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || E <= 0 || H <= 0) return MOE_ERR_INVALID;
+  if (H % 4) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!y || (k > 0 && (!d2 || !topk_ids || !topk_w || !g_down))) return MOE_ERR_INVALID;
+  if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
+  return status_of(launch_scatter(d2, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
+}
+
+size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I) {
+  if (T < 0 || k < 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+  return carve_layer(nullptr, T, k, E, H, I).bytes;
+}
+
+int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w, int k,
+                    const moe_nvfp4_weights_t* w, void* workspace, size_t ws_bytes, uint16_t* y,
+                    cudaStream_t stream) {
+  if (!w || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
+    return MOE_ERR_INVALID;
+  if (H % 128 || I % 128) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
+  if (!w->w13_packed || !w->w13_sf || !w->g_gate_up || !w->w2_packed || !w->w2_sf || !w->g_down)
+    return MOE_ERR_INVALID;
+  if ((long long)T * k > (1LL << 30) || (long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
+  const int E = w->E;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return MOE_ERR_INVALID;
+  const LayerWs ws = carve_layer(workspace, T, k, E, H, I);
+  if (ws_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  const int S = T * k;
+  cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
+  if (err == cudaSuccess) err = launch_quantize(x, k, S, H, ws.groups, ws.xq, ws.xsf, stream);
+  if (err == cudaSuccess)
+    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_packed, w->w13_sf, E, 2 * I, H, ws.d13, st, stream);
+  if (err == cudaSuccess) err = launch_swiglu(ws.d13, S, I, ws.groups, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
+  if (err == cudaSuccess)
+    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_packed, w->w2_sf, E, H, I, ws.d2, st, stream);
+  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+  return status_of(err);
+}
+
+int nvfp4_swizzle_block_scales(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t stream) {
+  if (N < 0 || K <= 0) return MOE_ERR_INVALID;
+  if (K % 64) return MOE_ERR_SHAPE;
+  if (N == 0) return MOE_OK;
+  if (!linear || !swizzled) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(linear) % 4 || reinterpret_cast<uintptr_t>(swizzled) % 4) return MOE_ERR_INVALID;
+  return status_of(launch_swizzle(linear, N, K, swizzled, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Device-side NVFP4 codec: e2m1 element codes and e4m3 (E4M3FN) block scales.
+//
+// Rounding follows the reading stated with the C ABI (round to nearest, ties
+// to even, saturating): written here from the value sets, not from any
+// vendor conversion routine. The first rocket blog page ("The CUTLASS grouped
+// GEMM beats the scalar GEMV loop", section "Proof") checks the device
+// quantizer byte for byte against a host codec; this file is the device half
+// of that contract.
+#pragma once
+#include <cstdint>
+
+namespace moe {
+
+// e4m3 code -> fp32 (exact). E4M3FN: bias 7, subnormals m * 2^-9; the codes
+// produced here never include 0x7F (NaN).
+__device__ __forceinline__ float e4m3_decode(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xF, m = code & 0x7;
+  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// fp32 >= 0 -> e4m3 code, round to nearest even, saturating at 448 (0x7E).
+__device__ __forceinline__ uint32_t e4m3_encode(float v) {
+  if (!(v > 0.0f)) return 0u;
+  if (v >= 448.0f) return 0x7Eu;
+  if (v < 0.015625f) {                    // below 2^-6: subnormal grid, step 2^-9
+    return (uint32_t)rintf(v * 512.0f);   // exact scaling; rintf is half-to-even
+  }
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t keep = (b >> 20) & 0x7u;   // top 3 mantissa bits
+  const uint32_t rest = b & 0xFFFFFu;       // 20 dropped bits
+  uint32_t code = ((((b >> 23) & 0xFFu) - 120u) << 3) | keep;
+  if (rest > 0x80000u || (rest == 0x80000u && (keep & 1u))) code += 1u;  // carry may bump the exponent
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// fp32 -> e2m1 code (bit 3 = sign), nearest with ties to the even code,
+// saturating at 6. Grid {0, .5, 1, 1.5, 2, 3, 4, 6}; each midpoint belongs to
+// the neighbour whose code is even.
+__device__ __forceinline__ uint32_t e2m1_encode(float v) {
+  const float a = fabsf(v);
+  uint32_t m;
+  if (a <= 0.25f) m = 0;
+  else if (a < 0.75f) m = 1;
+  else if (a <= 1.25f) m = 2;
+  else if (a < 1.75f) m = 3;
+  else if (a <= 2.5f) m = 4;
+  else if (a < 3.5f) m = 5;
+  else if (a <= 5.0f) m = 6;
+  else m = 7;
+  return m | (signbit(v) ? 8u : 0u);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits) { return __uint_as_float(bits << 16); }
+
+// One 16-element block: scale code and 8 packed bytes (as two u32, element
+// 2j in the low nibble of byte j). `v` holds fp32 values exact in bf16.
+struct Nvfp4Block {
+  uint32_t scale;
+  uint32_t lo, hi;
+};
+
+__device__ __forceinline__ Nvfp4Block quantize16(const float* v) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  Nvfp4Block out;
+  out.scale = e4m3_encode(__fdiv_rn(amax, 6.0f));
+  const float d = e4m3_decode(out.scale);
+  out.lo = out.hi = 0u;
+  if (d == 0.0f) return out;              // underflowed block: all-zero codes
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out.lo |= e2m1_encode(__fdiv_rn(v[i], d)) << (4 * i);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out.hi |= e2m1_encode(__fdiv_rn(v[8 + i], d)) << (4 * i);
+  return out;
+}
+
+// Byte offset of scale (row m, column c) in a region of 128-row atoms with
+// Kc scale columns: atoms run along K, then along rows; inside an atom,
+// 16 bytes per row of a 32-row slab and 4 bytes per 32-row quarter.
+__device__ __forceinline__ uint32_t sf_atom_offset(uint32_t m, uint32_t c, uint32_t Kc) {
+  return ((m >> 7) * (Kc >> 2) + (c >> 2)) * 512u + (m & 31u) * 16u + ((m >> 5) & 3u) * 4u + (c & 3u);
+}
+
+}  // namespace moe

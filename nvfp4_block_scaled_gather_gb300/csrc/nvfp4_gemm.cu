@@ -1,0 +1,428 @@
+// NVFP4 x NVFP4 grouped GEMM on tcgen05 block-scaled MMA (sm_103a).
+//
+// Computes, for every group g (expert e) of the routed rows,
+//   d[r, n] = sum_k A[r, k] * W[e, n, k]       (dequantized values, alpha = 1)
+// which is the "grouped GEMM (w13, fused)" and "grouped GEMM (w2)" step of the
+// rocket blog page "The CUTLASS grouped GEMM beats the scalar GEMV loop at
+// every M" (section "What changed"). The pages ran CUTLASS's SM120 grouped
+// kernel with 128-row token tiles; this kernel is written for GB300 instead:
+//
+//  * Swap-AB. The weight tile is the MMA's A operand (M = 128 output features)
+//    and the group's tokens are the B operand (N = Mg rounded up to 16), so a
+//    decode group of one row costs a 16-wide MMA, not a 128-row tile. The
+//    second page ("Tiles below M=8") notes that the wasted token extent costs
+//    no HBM traffic; here it costs no tensor-core time either.
+//  * Persistent CTAs (one per SM) walk the ragged work list of
+//    (128-row activation block, 128-row weight tile) units in a fixed order;
+//    every unit streams its weight tile over the full K once.
+//  * Warp roles: warp 0 issues TMA (weights and activations, 128B-swizzled)
+//    plus bulk copies of the e4m3 scale atoms into an mbarrier ring; warp 1
+//    copies scales into tensor memory (tcgen05.cp) and issues
+//    tcgen05.mma.kind::mxf4nvf4 (scale vector 16) into a double-buffered
+//    TMEM accumulator; warps 2-5 drain TMEM (tcgen05.ld) to fp32 global.
+//  * Every wait is bounded; on expiry the kernel records MOE_ERR_TIMEOUT,
+//    drains its own copies, frees tensor memory and returns.
+// A row's result never depends on other rows: the K loop order is fixed and
+// each output column of the MMA depends only on its own token.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;            // weight rows per tile = MMA M
+constexpr int kStageKBytes = 128;   // K bytes per stage and row = 256 e2m1 values
+constexpr int kAtomBytes = 512;     // one scale atom: 128 rows x 4 scales (64 K values)
+constexpr int kATileBytes = kBM * kStageKBytes;  // 16 KB
+constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
+constexpr int kBBoxRows = 16;
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kSmemBytes = 232448;  // 227 KB, the sm_100-family opt-in maximum
+constexpr int kTmemCols = 512;
+
+struct GemmArgs {
+  const uint8_t* a_sf;
+  const uint8_t* w_sf;
+  float* d;
+  const int32_t* counts;
+  const int32_t* group_offsets;
+  const int32_t* group_expert;
+  const int32_t* group_sf_block;
+  int* status;
+  int N, K;
+  long long wait_budget;  // clock64 cycles a single wait may take
+};
+
+// ------------------------------- PTX helpers --------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
+// that TMA writes: rows of 128 bytes, 8-row groups 1024 bytes apart
+// (stride byte offset), descriptor version 1, swizzle mode 2 (128B).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Descriptor of one 512-byte scale atom for tcgen05.cp.32x128b: 32 rows of
+// 16 bytes, no swizzle, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_scales(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor, kind::mxf4nvf4: A and B e2m1 (format 1), both
+// K-major, e4m3 scales, M = 128, N = n (multiple of 16), dense K = 64.
+__device__ __forceinline__ uint32_t idesc_nvf4(int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+struct Ctl {
+  volatile int* abort_flag;
+  int* status;
+  long long budget;
+};
+
+// Bounded wait: false if this or another role gave up.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*c.abort_flag) return false;
+    if (clock64() - t0 > c.budget) {
+      *c.abort_flag = 1;
+      atomicExch(c.status, (int)MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, int G, int key) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(starts + mid) <= key) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One unit of work: 128-row activation block `chunk` (a group's rows
+// [128q, 128q + 128)) against 128-row weight tile `nt` of the group's expert.
+struct Unit {
+  int row0, nvalid, nmma, a_row, nt;
+  size_t sfa_off, sfb_off;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int G, int kc4) {
+  const int chunk = u / n_tiles;
+  Unit un;
+  un.nt = u - chunk * n_tiles;
+  const int gi = find_group(p.group_sf_block, G, chunk);
+  const int q = chunk - __ldg(p.group_sf_block + gi);
+  const int r0 = __ldg(p.group_offsets + gi);
+  const int mg = __ldg(p.group_offsets + gi + 1) - r0;
+  const int e = __ldg(p.group_expert + gi);
+  un.row0 = r0 + kBM * q;
+  un.nvalid = min(kBM, mg - kBM * q);
+  un.nmma = (un.nvalid + 15) & ~15;
+  un.a_row = e * p.N + un.nt * kBM;
+  un.sfa_off = ((size_t)e * n_tiles + un.nt) * kc4 * kAtomBytes;
+  un.sfb_off = (size_t)chunk * kc4 * kAtomBytes;
+  return un;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain[1]
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- schedule shape, identical on every thread ----
+  const int G = __ldg(p.counts + 0);
+  const int maxmg = __ldg(p.counts + 2);
+  const int nblk = G > 0 ? __ldg(p.group_sf_block + G) : 0;
+  const int n_tiles = p.N / kBM;
+  const int total_units = nblk * n_tiles;
+  const int kc4 = p.K / 64;               // scale atoms along K per 128-row block
+  const int nk = (p.K + 255) / 256;       // stages per unit
+  const int tn = min(kBM, max(16, (maxmg + 15) & ~15));   // token rows per B stage
+  const int acc_cols = max(32, tn);
+  const int stage_bytes = kATileBytes + tn * kStageKBytes + 2 * kSfStageBytes;
+  const int avail = kSmemBytes - 1024 - 1024;
+  int stages = min(kMaxStages, avail / stage_bytes);
+  stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
+  const uint32_t sA = smem_u32(smem + 1024);
+  const uint32_t sB = sA + (uint32_t)stages * kATileBytes;
+  const uint32_t sSFA = sB + (uint32_t)stages * tn * kStageKBytes;
+  const uint32_t sSFB = sSFA + (uint32_t)stages * kSfStageBytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Ctl ctl{abort_flag, p.status, p.wait_budget};
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0 && total_units > 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, fill_parity = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+        const int nbox = un.nmma / kBBoxRows;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
+          const int natoms = min(4, kc4 - 4 * ks);
+          const uint32_t bytes = kATileBytes + nbox * kBBoxRows * kStageKBytes + 2u * natoms * kAtomBytes;
+          const uint32_t fb = full_bar(stage);
+          mbar_expect_tx(fb, bytes);
+          tma_load_2d(sA + stage * kATileBytes, &tmA, ks * kStageKBytes, un.a_row, fb);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, &tmB, ks * kStageKBytes,
+                        un.row0 + b * kBBoxRows, fb);
+          bulk_load(sSFA + stage * kSfStageBytes, p.w_sf + un.sfa_off + (size_t)ks * kSfStageBytes,
+                    natoms * kAtomBytes, fb);
+          bulk_load(sSFB + stage * kSfStageBytes, p.a_sf + un.sfb_off + (size_t)ks * kSfStageBytes,
+                    natoms * kAtomBytes, fb);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let every copy this thread issued land before the CTA exits
+        for (int s = 0; s < stages; ++s)
+          if (filled & (1u << s)) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(full_bar(s), (fill_parity >> s) & 1u) && clock64() - t0 < ctl.budget) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================= MMA issuer =============================
+    if (lane == 0 && total_units > 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+        if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
+        const uint32_t idesc = idesc_nvf4(un.nmma);
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const int natoms = min(4, kc4 - 4 * ks);
+          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+          for (int a = 0; a < natoms; ++a) {
+            tc_cp_scales(sf_col + 4 * a, desc_scales(sSFA + stage * kSfStageBytes + a * kAtomBytes));
+            tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
+          }
+          for (int a = 0; a < natoms; ++a) {
+            const uint64_t adesc = desc_sw128(sA + stage * kATileBytes + 32 * a);
+            const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        // wait for every MMA / scale copy issued so far before TMEM is freed
+        tc_commit(drain_bar);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < ctl.budget) {
+        }
+      }
+    }
+  } else {
+    // ============================== epilogue ==============================
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+      if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
+      tc_fence_after();
+      const int n = un.nt * kBM + quad * 32 + lane;
+      float* dcol = p.d + (size_t)un.row0 * p.N + n;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
+      for (int c0 = 0; c0 < un.nvalid; c0 += 16) {
+        uint32_t r[16];
+        tc_ld_32x32b_x16(taddr + c0, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < un.nvalid) dcol[(size_t)(c0 + j) * p.N] = __uint_as_float(r[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(acce_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows, row_bytes] read in 128-byte x box_rows boxes with
+// the 128-byte swizzle (zero fill out of bounds).
+bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kStageKBytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
+                                const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K, float* d,
+                                int* status, cudaStream_t s) {
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, w_packed, (uint64_t)K / 2, (uint64_t)E * N, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
+  GemmArgs p;
+  p.a_sf = a_sf;
+  p.w_sf = w_sf;
+  p.d = d;
+  p.counts = g.counts;
+  p.group_offsets = g.group_offsets;
+  p.group_expert = g.group_expert;
+  p.group_sf_block = g.group_sf_block;
+  p.status = status;
+  p.N = N;
+  p.K = K;
+  p.wait_budget = 2000000000LL;
+  cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const long long units_bound = sf_blocks_bound(R_max, E < R_max ? E : R_max) * (N / kBM);
+  const int grid = (int)(units_bound < num_sms() ? units_bound : num_sms());
+  gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

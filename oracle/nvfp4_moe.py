@@ -274,7 +274,7 @@ def grouped_gemm(a_packed, a_sf, group_offsets, group_expert, w_packed, w_sf_lin
     groups. Products of e2m1*e4m3 values are exact in fp64; the fp64 sum is
     the exact value to within fp64 rounding."""
     A = dequantize_rows(a_packed, a_sf, group_offsets)
-    N = np.asarray(w_packed).shape[1]
+    N = w_packed.shape[1]  # w_packed / w_sf_linear: anything indexable by expert id
     D = np.zeros((A.shape[0], N), dtype=np.float64)
     offs = np.asarray(group_offsets, dtype=np.int64)
     for g, e in enumerate(np.asarray(group_expert, dtype=np.int64)):

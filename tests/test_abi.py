@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point the header declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_block_scaled_gather_gb300 import _native
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_nvfp4.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_hot_path():
+    names = set(declared_functions())
+    for n in ("moe_gather_rows", "nvfp4_quantize_rows", "nvfp4_grouped_gemm", "swiglu_grouped",
+              "moe_scatter_add", "moe_nvfp4_layer", "moe_nvfp4_layer_workspace_size",
+              "nvfp4_swizzle_block_scales", "moe_route_groups"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(native):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(native, n), n
+    assert set(names) == set(_native.exported_symbols())
+
+
+def test_error_strings(native):
+    for code in range(6):
+        assert native.moe_nvfp4_error_string(code)
+    assert native.moe_nvfp4_error_string(0) == b"ok"
+
+
+def _fake_groups():
+    g = _native.MoeGroups()
+    for name, _ in g._fields_:
+        setattr(g, name, 4096)
+    return g
+
+
+def test_host_side_validation(native):
+    g = _fake_groups()
+    s = None
+    # unsupported GEMM shapes
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 16, 4, 100, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 16, 4, 128, 96, 16, s) == 2
+    # missing group arrays / bad sizes
+    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 16, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_quantize_rows(16, 8, 100, ctypes.byref(g), 16, 16, s) == 2
+    assert native.moe_route_groups(16, 2, 2, 2000, ctypes.byref(g), s) == 1
+    assert native.moe_route_groups(16, 2, 40, 8, ctypes.byref(g), s) == 1
+    assert native.moe_scatter_add(16, 256, 16, 16, 2, 2, -1, ctypes.byref(g), 16, 16, s) == 1
+    w = _native.MoeWeights(8, 16, 16, 16, 16, 16, 16)
+    assert native.moe_nvfp4_layer(16, 4, 200, 128, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
+    assert native.moe_nvfp4_layer(16, 4, 256, 96, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
+    assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, None, 256, 1 << 20, 16, s) == 1
+    ws = native.moe_nvfp4_layer_workspace_size(4, 2, 8, 256, 128)
+    assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 256, ws - 1, 16, s) == 5
+    assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 300, ws, 16, s) == 1
+    # empty problems are no-ops
+    assert native.moe_nvfp4_layer(None, 0, 256, 128, None, None, 2, ctypes.byref(w), None, 0, None, s) == 0
+    assert native.nvfp4_swizzle_block_scales(None, 0, 64, None, s) == 0
+
+
+def test_sizes(native):
+    assert native.moe_groups_bytes(1, 8, 288) > 0
+    # sf region bound: (min(E, R) + ceil(R / 128)) * 128 * K / 16
+    assert native.nvfp4_sf_bytes(8, 288, 4096) == (8 + 1) * 128 * 256
+    assert native.nvfp4_sf_bytes(2304, 288, 2048) == (288 + 18) * 128 * 128
+    small = native.moe_nvfp4_layer_workspace_size(1, 8, 288, 4096, 2048)
+    big = native.moe_nvfp4_layer_workspace_size(288, 8, 288, 4096, 2048)
+    assert 0 < small < big
+
+
+def test_groups_carve_is_host_only(native):
+    buf = ctypes.create_string_buffer(native.moe_groups_bytes(3, 2, 5) + 512)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    g = _native.MoeGroups()
+    assert native.moe_groups_carve(base, 3, 2, 5, ctypes.byref(g)) == 0
+    assert g.counts == base and g.slot_row > g.row_slot > g.group_offsets
+    assert native.moe_groups_carve(base + 4, 3, 2, 5, ctypes.byref(g)) == 1

@@ -1,0 +1,326 @@
+"""CUDA path (through the C ABI) against the CPU oracle, step by step and end
+to end, at the thresholds the layer is held to:
+  * bit-exact: grouping (row order, offsets, group order), gathered rows,
+    packed nibbles and scale bytes (padding included), requantized h;
+  * grouped GEMM: relative Frobenius error <= 1e-5 against the oracle fed the
+    same quantized inputs;
+  * SwiGLU h and scatter y: within one bf16 unit in the last place of the
+    oracle fed the same GEMM outputs (fp32 on the device, fp64 in the oracle);
+  * layer output: relative Frobenius error <= 1e-2 (a 1-ulp difference in h can
+    flip an e2m1 code at requantization).
+"""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_block_scaled_gather_gb300 import _native as N
+from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_layer, make_weights, make_activations, \
+    make_routing
+from oracle import nvfp4_moe as O
+from tests.gpu_cases import (LazyExperts, bf16_to_np, bf16_ulps, np_to_bf16, oracle_weights, rel_fro, run_stages,
+                             small_case, weights_from)
+
+pytestmark = pytest.mark.gpu
+
+GEMM_TOL = 1e-5
+LAYER_TOL = 1e-2
+
+
+def np_inputs(x, ids, tw):
+    return bf16_to_np(x), ids.cpu().numpy(), tw.cpu().numpy()
+
+
+def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
+    G = len(ref_gexp)
+    assert host["G"] == G and host["R"] == len(ref_row_slot)
+    assert np.array_equal(host["group_expert"].numpy(), ref_gexp)
+    assert np.array_equal(host["group_offsets"].numpy(), ref_offs)
+    assert np.array_equal(host["row_slot"].numpy(), ref_row_slot)
+    assert np.array_equal(host["group_sf_block"].numpy(), O.group_sf_blocks(ref_offs))
+    assert host["max_mg"] == (int(np.diff(ref_offs).max()) if G else 0)
+    slot_row = np.full(S, -1)
+    slot_row[ref_row_slot] = np.arange(len(ref_row_slot))
+    assert np.array_equal(host["slot_row"].numpy(), slot_row)
+
+
+def check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, H, I):
+    """Each stage of a run_stages() result against the oracle fed the GPU's
+    own inputs for that stage."""
+    T, k = ids_np.shape
+    row_slot, offs, gexp = O.route_groups(ids_np, E)
+    check_groups(st["groups"], row_slot, offs, gexp, T * k)
+    R = len(row_slot)
+    xg = O.gather_rows(x_np, row_slot, k)
+    assert np.array_equal(bf16_to_np(st["xg"])[:R], xg)
+    xq, xsf = O.quantize_rows(xg, offs)
+    assert np.array_equal(st["xq"][:R].cpu().numpy(), xq)
+    assert np.array_equal(st["xsf"][:xsf.size].cpu().numpy(), xsf)
+    d13 = O.grouped_gemm(xq, xsf, offs, gexp, w_np["w13_packed"], w_np["w13_sf_linear"])
+    assert rel_fro(st["d13"][:R].cpu().numpy(), d13) <= GEMM_TOL
+    h_ref = O.swiglu(st["d13"][:R].cpu().numpy().astype(np.float64), offs, gexp, w_np["g_gate_up"])
+    assert bf16_ulps(bf16_to_np(st["h"])[:R], h_ref).max() <= 1
+    h_gpu = bf16_to_np(st["h"])[:R]
+    hq, hsf = O.quantize_rows(h_gpu, offs)
+    assert np.array_equal(st["hq"][:R].cpu().numpy(), hq)
+    assert np.array_equal(st["hsf"][:hsf.size].cpu().numpy(), hsf)
+    d2 = O.grouped_gemm(hq, hsf, offs, gexp, w_np["w2_packed"], w_np["w2_sf_linear"])
+    assert rel_fro(st["d2"][:R].cpu().numpy(), d2) <= GEMM_TOL
+    y_ref = O.scatter_add(st["d2"][:R].cpu().numpy().astype(np.float64), row_slot, ids_np, tw_np,
+                          w_np["g_down"], T, E)
+    assert bf16_ulps(bf16_to_np(st["y"]), y_ref).max() <= 1
+
+
+# ---------------------------------------------------------------------------
+# tiny config (BASELINE tiny layer: 8 experts, hidden 256, intermediate 128)
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def tiny(cuda):
+    cfg = CONFIGS["tiny"]
+    inp = make_layer(cfg, device="cpu")
+    w_np = {k: inp[k].numpy() for k in ("w13_packed", "w13_sf_linear", "g_gate_up", "w2_packed", "w2_sf_linear",
+                                        "g_down")}
+    x_np, ids_np, tw_np = np_inputs(inp["x"], inp["topk_ids"], inp["topk_w"])
+    ref = O.moe_layer(x_np, ids_np, tw_np, w_np, E=cfg.E)
+    gpu = {k: (v.to(cuda) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    W = weights_from(gpu)
+    return cfg, gpu, W, w_np, (x_np, ids_np, tw_np), ref
+
+
+def test_tiny_stages(tiny):
+    cfg, g, W, w_np, (x_np, ids_np, tw_np), _ = tiny
+    st = run_stages(g["x"], g["topk_ids"], g["topk_w"], W, cfg.E)
+    check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, cfg.E, cfg.H, cfg.I)
+    assert N.check_status() == 0
+
+
+def test_tiny_layer_end_to_end(tiny):
+    cfg, g, W, _, _, ref = tiny
+    layer = N.MoeLayer(W, T_max=g["x"].shape[0], k=cfg.k)
+    y = layer(g["x"], g["topk_ids"], g["topk_w"])
+    torch.cuda.synchronize()
+    assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(y)), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
+    assert N.check_status() == 0
+
+
+def test_tiny_layer_equals_stages(tiny):
+    cfg, g, W, *_ = tiny
+    st = run_stages(g["x"], g["topk_ids"], g["topk_w"], W, cfg.E)
+    y = N.MoeLayer(W, g["x"].shape[0], cfg.k)(g["x"], g["topk_ids"], g["topk_w"])
+    assert torch.equal(y.view(torch.int16), st["y"].view(torch.int16))
+
+
+def test_swizzle_matches_oracle(cuda):
+    rng = np.random.default_rng(31)
+    for n, kk in ((256, 256), (384, 512), (100, 128)):
+        lin = rng.integers(0, 256, (n, kk // 16), dtype=np.uint8)
+        out = torch.zeros(((n + 127) // 128) * 128 * kk // 16, dtype=torch.uint8, device=cuda)
+        N.nvfp4_swizzle_block_scales(torch.from_numpy(lin).to(cuda), out)
+        assert np.array_equal(out.cpu().numpy(), O.swizzle_scales(lin))
+
+
+# ---------------------------------------------------------------------------
+# codec edge cases, and the pages' group_m = {1, 130} quantizer case
+# ---------------------------------------------------------------------------
+
+def _groups_for(mg, cuda):
+    """Routing with k = 1 giving groups of the given sizes (experts 0..)."""
+    ids = torch.cat([torch.full((m,), e, dtype=torch.int32) for e, m in enumerate(mg)]).reshape(-1, 1)
+    G = N.Groups(ids.shape[0], 1, len(mg), cuda)
+    N.moe_route_groups(ids.to(cuda), len(mg), G)
+    return ids, G
+
+
+def edge_rows(R, K, seed=0):
+    """bf16 rows mixing N(0,1), wide dynamic range, e2m1 ties, e4m3 subnormal
+    and saturating scales, all-zero and underflowing (signed) blocks."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((R, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-14, 12, (R, K // 16))).repeat(16, axis=1).astype(np.float32)
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
+    for r in range(R):
+        c = 16 * int(rng.integers(0, K // 16))
+        x[r, c:c + 16] = np.tile(ties, 2) * rng.choice([-1, 1], 16)  # amax 6 -> scale 1, exact ties
+    x[0, :16] = 0.0
+    x[min(1, R - 1), :16] = -1e-7
+    x[min(2, R - 1), 16:32] = 5000.0                                    # scale saturates at 448
+    x[min(3, R - 1), 32:48] = 2.0 ** -9 * np.arange(16)                  # subnormal scale
+    return np.asarray(O.f64_to_bf16_bits(x.astype(np.float64)))
+
+
+@pytest.mark.parametrize("mg,K", [((1, 130), 64), ((3, 17, 1, 140), 256), ((1,), 4096)])
+def test_quantize_rows_bit_exact(cuda, mg, K):
+    R = sum(mg)
+    rows = edge_rows(R, K, seed=R + K)
+    _, G = _groups_for(mg, cuda)
+    offs = np.concatenate([[0], np.cumsum(mg)])
+    packed = torch.zeros(R, K // 2, dtype=torch.uint8, device=cuda)
+    sf = torch.full((N.sf_bytes(R, len(mg), K),), 0xAB, dtype=torch.uint8, device=cuda)
+    N.nvfp4_quantize_rows(np_to_bf16(rows, cuda), G, packed, sf)
+    ref_p, ref_sf = O.quantize_rows(rows, offs)
+    assert np.array_equal(packed.cpu().numpy(), ref_p)
+    assert np.array_equal(sf[:ref_sf.size].cpu().numpy(), ref_sf)
+    if mg == (1, 130):
+        assert ref_p.nbytes + ref_sf.nbytes == 5728
+
+
+def test_gather_quantize_fused_equals_separate(cuda):
+    E, x, ids, tw, w = small_case("cpu")
+    x, ids = x.to(cuda), ids.to(cuda)
+    T, H = x.shape
+    k, S = ids.shape[1], ids.numel()
+    G = N.Groups(T, k, E, cuda)
+    xg = torch.zeros(S, H, dtype=torch.bfloat16, device=cuda)
+    N.moe_gather_rows(x, ids, E, G, xg)
+    p1 = torch.zeros(S, H // 2, dtype=torch.uint8, device=cuda)
+    s1 = torch.zeros(N.sf_bytes(S, E, H), dtype=torch.uint8, device=cuda)
+    p2, s2 = p1.clone(), s1.clone()
+    N.nvfp4_quantize_rows(xg, G, p1, s1)
+    N.moe_gather_quantize_rows(x, k, G, p2, s2)
+    assert torch.equal(p1, p2) and torch.equal(s1, s2)
+
+
+# ---------------------------------------------------------------------------
+# several tiles, ragged tails, a group spanning two 128-row blocks
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def small(cuda):
+    E, x, ids, tw, w = small_case("cpu")
+    w_np = {k: v.numpy() for k, v in w.items()}
+    gpu = {k: v.to(cuda) for k, v in w.items()}
+    return E, x.to(cuda), ids.to(cuda), tw.to(cuda), weights_from(gpu), w_np, np_inputs(x, ids, tw)
+
+
+def test_small_stages(small):
+    E, x, ids, tw, W, w_np, (x_np, ids_np, tw_np) = small
+    st = run_stages(x, ids, tw, W, E)
+    check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, W.H, W.I)
+
+
+def test_small_layer_end_to_end(small):
+    E, x, ids, tw, W, w_np, (x_np, ids_np, tw_np) = small
+    y = N.MoeLayer(W, x.shape[0], ids.shape[1])(x, ids, tw)
+    ref = O.moe_layer(x_np, ids_np, tw_np, w_np, E)
+    assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(y)), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
+    # a token with every slot unused gets zeros; check_status stays clean
+    assert N.check_status() == 0
+
+
+def test_gemm_row_invariance_and_fused_w13(small):
+    """First page, "Proof": a row alone equals the same row paired; fused w13
+    equals separate gate-only and up-only GEMMs; five calls bit-identical.
+    Here also across MMA widths: the 140-row group runs a 128-wide and a
+    16-wide MMA, the row alone a 16-wide one."""
+    E, x, ids, tw, W, *_ = small
+    st = run_stages(x, ids, tw, W, E)
+    dev = x.device
+    I = W.I
+    hostg = st["groups"]
+    # rows of expert 0 (group 0, 140 rows): compare row 0, row 127, row 130 alone
+    for r in (0, 127, 130, 139):
+        xa = st["xg"][r:r + 1]
+        G1 = N.Groups(1, 1, E, dev)
+        N.moe_route_groups(torch.zeros((1, 1), dtype=torch.int32, device=dev), E, G1)
+        q = torch.zeros(1, W.H // 2, dtype=torch.uint8, device=dev)
+        s = torch.zeros(N.sf_bytes(1, E, W.H), dtype=torch.uint8, device=dev)
+        N.nvfp4_quantize_rows(xa, G1, q, s)
+        d = torch.zeros(1, 2 * I, dtype=torch.float32, device=dev)
+        N.nvfp4_grouped_gemm(q, s, G1, W.w13_packed, W.w13_sf, d)
+        assert torch.equal(d[0], st["d13"][r]), r
+    # fused w13 == gate-only and up-only (gate's scale region then up's)
+    G = N.Groups(x.shape[0], ids.shape[1], E, dev)
+    N.moe_route_groups(ids, E, G)
+    R_max = ids.numel()
+    half = W.w13_sf.shape[1] // 2
+    gate = torch.zeros(R_max, I, dtype=torch.float32, device=dev)
+    up = torch.zeros(R_max, I, dtype=torch.float32, device=dev)
+    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed[:, :I].contiguous(),
+                         W.w13_sf[:, :half].contiguous(), gate)
+    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed[:, I:].contiguous(),
+                         W.w13_sf[:, half:].contiguous(), up)
+    R = hostg["R"]
+    assert torch.equal(torch.cat([gate, up], 1)[:R], st["d13"][:R])
+    for _ in range(5):
+        d = torch.zeros_like(st["d13"])
+        N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed, W.w13_sf, d)
+        assert torch.equal(d[:R], st["d13"][:R])
+
+
+def test_swiglu_requant_fused_equals_separate(small):
+    E, x, ids, tw, W, *_ = small
+    st = run_stages(x, ids, tw, W, E)
+    G = N.Groups(x.shape[0], ids.shape[1], E, x.device)
+    N.moe_route_groups(ids, E, G)
+    p = torch.zeros_like(st["hq"])
+    s = torch.zeros_like(st["hsf"])
+    N.swiglu_quantize_grouped(st["d13"], G, W.g_gate_up, p, s)
+    R = st["groups"]["R"]
+    assert torch.equal(p[:R], st["hq"][:R]) and torch.equal(s, st["hsf"])
+
+
+def test_layer_determinism_and_batch_invariance(small):
+    E, x, ids, tw, W, *_ = small
+    layer = N.MoeLayer(W, x.shape[0], ids.shape[1])
+    y0 = layer(x, ids, tw).clone()
+    for _ in range(4):
+        assert torch.equal(layer(x, ids, tw).view(torch.int16), y0.view(torch.int16))
+    for t in (0, 7, 100, 141, 150, 159):
+        yt = layer(x[t:t + 1].contiguous(), ids[t:t + 1].contiguous(), tw[t:t + 1].contiguous())
+        assert torch.equal(yt[0].view(torch.int16), y0[t].view(torch.int16)), t
+
+
+def test_unused_slots_and_empty(cuda, tiny):
+    cfg, g, W, *_ = tiny
+    x = g["x"]
+    ids = torch.full_like(g["topk_ids"], -1)
+    y = torch.full_like(x, 7.0)
+    N.MoeLayer(W, x.shape[0], cfg.k)(x, ids, g["topk_w"], y)
+    assert not y.float().abs().sum().item()
+    # T = 0 is a no-op
+    N.moe_nvfp4_layer(x[:0], g["topk_ids"][:0], g["topk_w"][:0], W, torch.empty(256, dtype=torch.uint8,
+                                                                                   device=cuda), x[:0])
+    assert N.check_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# full-size layer (288 experts, hidden 4096, intermediate 2048): every step at
+# the configs' sizes, checked on sampled tokens against the oracle run on those
+# tokens alone (valid because a token's output does not depend on the batch)
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def full_weights(cuda):
+    cfg = CONFIGS["decode_m1"]
+    w = make_weights(cfg.E, cfg.H, cfg.I, device=cuda)
+    return w, weights_from(w), oracle_weights(w)
+
+
+def _token_check(t, x_np, ids_np, tw_np, w_or, E, gpu_y, gpu_st=None):
+    ref = O.moe_layer(x_np[t:t + 1], ids_np[t:t + 1], tw_np[t:t + 1], w_or, E)
+    assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(gpu_y[t:t + 1])), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
+    if gpu_st is not None:
+        k = ids_np.shape[1]
+        slot_row = gpu_st["groups"]["slot_row"].numpy()
+        rows = [slot_row[t * k + s] for s in ref["row_slot"]]
+        assert rel_fro(gpu_st["d13"][rows].cpu().numpy(), ref["d13"]) <= GEMM_TOL
+        assert np.array_equal(gpu_st["xq"][rows].cpu().numpy(), ref["xq"])
+
+
+@pytest.mark.parametrize("name,tokens", [("decode_m1", (0,)), ("decode_m8", (0, 5)), ("decode_m32", (3, 31)),
+                                         ("full_stream", (0, 40)), ("large_batch", (1, 150, 287))])
+def test_full_size_layer(cuda, full_weights, name, tokens):
+    cfg = CONFIGS[name]
+    w, W, w_or = full_weights
+    ids, tw = make_routing(cfg)
+    x = make_activations(ids.shape[0], cfg.H, device=cuda)
+    ids_d, tw_d = ids.to(cuda), tw.to(cuda)
+    y = N.MoeLayer(W, ids.shape[0], cfg.k)(x, ids_d, tw_d)
+    st = run_stages(x, ids_d, tw_d, W, cfg.E)
+    assert torch.equal(y.view(torch.int16), st["y"].view(torch.int16))
+    x_np, ids_np, tw_np = np_inputs(x, ids, tw)
+    row_slot, offs, gexp = O.route_groups(ids_np, cfg.E)
+    check_groups(st["groups"], row_slot, offs, gexp, ids.numel())
+    for t in tokens:
+        _token_check(t, x_np, ids_np, tw_np, w_or, cfg.E, y, st)
+    assert N.check_status() == 0
