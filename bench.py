@@ -1,0 +1,539 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 routed-expert MoE layer step on GB300.
+
+One step = one moe_nvfp4_layer call (route-group, gather+quantize, grouped
+GEMM w13, SwiGLU+requantize, grouped GEMM w2, scatter-add) over one batch of
+synthetic input already resident in HBM. The L2 is flushed (a write of twice
+its size) before every timed step and the routing rotates over 20 seeded
+draws, so weights always stream from HBM.
+
+Prints one JSON line. value = weight-stream GB/s: algorithmic bytes per step
+(active experts' packed weights + block scales, x, y, routing, globals) over
+the mean device time of a step. `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer ms/step and weight-stream GB/s (% of HBM roofline) at M=1/8/32"
+FALLBACK_HBM_GBS = 6800.0
+N_ROUTINGS = 20
+GEMM_SRC = os.path.join(ROOT, "nvfp4_block_scaled_gather_gb300", "csrc", "nvfp4_gemm.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_w13_decode_m1_traffic.txt")
+
+
+def expert_bytes(H, I):
+    """Packed e2m1 + e4m3 block scales of one expert: w13 2I x H, w2 H x I."""
+    return 3 * H * I * 9 // 16
+
+
+def step_bytes(cfg, G, T):
+    """Algorithmic bytes of one layer step: active experts' weights, x read,
+    y written, routing ids + weights, per-expert globals."""
+    return G * expert_bytes(cfg.H, cfg.I) + 2 * T * cfg.H * 2 + T * cfg.k * 8 + 12 * cfg.E
+
+
+def w13_launch_bytes(cfg, G, R):
+    """Algorithmic bytes of one w13 grouped-GEMM launch: the active experts'
+    w13 (2I x H e2m1 + scales), the NVFP4 activation rows and their scales,
+    the fp32 output rows."""
+    return G * 2 * cfg.I * cfg.H * 9 // 16 + R * cfg.H * 9 // 16 + R * 2 * cfg.I * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if key in d:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """ncu DRAM bytes per w13 launch (decode M=1), if recorded for the current
+    kernel source; None when absent or when the kernel changed since."""
+    try:
+        with open(GEMM_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    a, b = line.split(":", 1)
+                    kv[a.strip()] = b.strip()
+        if kv.get("kernel_source_sha256_16") == sha:
+            return int(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def wait_first(self):
+        """Blocks until nvidia-smi printed its first sample (or exited)."""
+        self._first = self.proc.stdout.readline() if self.proc else None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        lines = [ln for ln in ((self._first or "") + out).splitlines() if ln.strip()]
+        sm, mx, reasons = [], 0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, parts[2:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_bench(args, rank, world):
+    import torch
+
+    from nvfp4_block_scaled_gather_gb300 import _native as N
+    from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_activations, make_routing, make_weights
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+    N.load()
+
+    cfg = CONFIGS[args.config]
+    if args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, E=args.experts)
+    w = make_weights(cfg.E, cfg.H, cfg.I, device=dev)
+    W = N.Weights(w["w13_packed"], w["w13_sf_linear"], w["g_gate_up"], w["w2_packed"], w["w2_sf_linear"],
+                  w["g_down"])
+    del w
+    flush = torch.empty(2 * props.L2_cache_size, dtype=torch.uint8, device=dev)
+
+    def workload(c, n=N_ROUTINGS):
+        items = []
+        for i in range(n):
+            ids, tw = make_routing(c, seed=2 + 1000 * i)
+            T = ids.shape[0]
+            x = make_activations(T, c.H, seed=1 + 1000 * i, device=dev)
+            valid = ids[(ids >= 0) & (ids < c.E)]
+            G = int(torch.unique(valid).numel())
+            items.append(dict(x=x, ids=ids.to(dev), tw=tw.to(dev), ids_h=ids, tw_h=tw, T=T, G=G,
+                              R=int(valid.numel())))
+        return items
+
+    def time_layer(c, items, steps, warmup, sampler=None):
+        T_max = max(it["T"] for it in items)
+        layer = N.MoeLayer(W, T_max, c.k)
+        ys = [torch.empty_like(it["x"]) for it in items]
+        for i in range(warmup):
+            it = items[i % len(items)]
+            layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+        if sampler is not None:
+            # keep the clocks sampler busy for at least ~1 s of load before timing
+            t0 = time.time()
+            i = 0
+            while time.time() - t0 < 1.0:
+                it = items[i % len(items)]
+                flush.zero_()
+                layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+                i += 1
+                if i % 20 == 0:
+                    torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            it = items[i % len(items)]
+            flush.zero_()
+            ev[i][0].record(stream)
+            layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        byts = [step_bytes(c, items[i % len(items)]["G"], items[i % len(items)]["T"]) for i in range(steps)]
+        return ms, byts
+
+    def time_stages(c, items, steps):
+        """Same kernels as the fused entry, launched stage by stage with
+        events between them (per-kernel device time)."""
+        T_max = max(it["T"] for it in items)
+        S = T_max * c.k
+        G_ = N.Groups(T_max, c.k, c.E, dev)
+        xq = torch.empty(S, c.H // 2, dtype=torch.uint8, device=dev)
+        xsf = torch.empty(N.sf_bytes(S, c.E, c.H), dtype=torch.uint8, device=dev)
+        d13 = torch.empty(S, 2 * c.I, dtype=torch.float32, device=dev)
+        hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
+        hsf = torch.empty(N.sf_bytes(S, c.E, c.I), dtype=torch.uint8, device=dev)
+        d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
+        names = ["route", "gather_quantize", "gemm_w13", "swiglu_quantize", "gemm_w2", "scatter"]
+        acc = {n: [] for n in names}
+        w13_bytes = []
+        for i in range(steps + 3):
+            it = items[i % len(items)]
+            T = it["T"]
+            G1 = N.Groups(T, c.k, c.E, dev) if T != T_max else G_
+            y = torch.empty_like(it["x"])
+            flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+            evs[0].record(stream)
+            N.moe_route_groups(it["ids"], c.E, G1)
+            evs[1].record(stream)
+            N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf)
+            evs[2].record(stream)
+            N.nvfp4_grouped_gemm(xq, xsf, G1, W.w13_packed, W.w13_sf, d13)
+            evs[3].record(stream)
+            N.swiglu_quantize_grouped(d13, G1, W.g_gate_up, hq, hsf)
+            evs[4].record(stream)
+            N.nvfp4_grouped_gemm(hq, hsf, G1, W.w2_packed, W.w2_sf, d2)
+            evs[5].record(stream)
+            N.moe_scatter_add(d2, it["ids"], it["tw"], c.E, G1, W.g_down, y)
+            evs[6].record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                for j, n in enumerate(names):
+                    acc[n].append(evs[j].elapsed_time(evs[j + 1]))
+                w13_bytes.append(w13_launch_bytes(c, it["G"], it["R"]))
+        return {n: statistics.mean(v) for n, v in acc.items()}, statistics.mean(w13_bytes)
+
+    def time_e2e(c, items, steps):
+        """Through the public call with host buffers: pinned H2D of x, ids and
+        router weights, the layer, D2H of y; all inside the timed region."""
+        T_max = max(it["T"] for it in items)
+        layer = N.MoeLayer(W, T_max, c.k)
+        host = []
+        for it in items:
+            host.append(dict(x=it["x"].cpu().pin_memory(), ids=it["ids_h"].pin_memory(),
+                             tw=it["tw_h"].pin_memory(), y=torch.empty_like(it["x"], device="cpu").pin_memory(),
+                             T=it["T"], G=it["G"]))
+        ms, h2d, d2h, byts = [], [], [], []
+        for i in range(steps + 3):
+            h = host[i % len(host)]
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            x = h["x"].to(dev, non_blocking=True)
+            ids = h["ids"].to(dev, non_blocking=True)
+            tw = h["tw"].to(dev, non_blocking=True)
+            y = layer(x, ids, tw)
+            h["y"].copy_(y, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+                h2d.append(x.numel() * 2 + ids.numel() * 4 + tw.numel() * 4)
+                d2h.append(y.numel() * 2)
+                byts.append(step_bytes(c, h["G"], h["T"]))
+        return ms, byts, statistics.mean(h2d), statistics.mean(d2h)
+
+    try:
+        gpu_id = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        gpu_id = str(local)
+    items = workload(cfg)
+    if args.profile:
+        # short run for profilers: warm-up, then the timed steps, nothing else
+        ms, byts = time_layer(cfg, items, args.steps, args.warmup)
+        print(json.dumps({"profile_run": cfg.name, "experts": cfg.E, "ms_per_step": statistics.mean(ms)}))
+        return
+    sampler = ClockSampler(gpu_id)
+    sampler.wait_first()
+    ms, byts = time_layer(cfg, items, args.steps, args.warmup, sampler)
+    clocks = sampler.stop()
+    if dist:
+        t = torch.tensor([sum(ms)], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    else:
+        total_ms = sum(ms)
+    ms_step = total_ms / args.steps
+    gbs = world * sum(byts) / (total_ms * 1e-3) / 1e9
+
+    stages, w13_bytes = time_stages(cfg, items, max(5, min(args.steps, 20)))
+    peak, peak_kind = measured_peaks()
+    achieved = w13_bytes / (stages["gemm_w13"] * 1e-3) / 1e9
+    e2e_ms, e2e_bytes, h2d, d2h = time_e2e(cfg, items, max(5, min(args.steps, 20)))
+    e2e_gbs = world * sum(e2e_bytes) / (sum(e2e_ms) * 1e-3) / 1e9
+
+    per_config = {}
+    if world == 1 and not args.no_extra:
+        for name in args.extra.split(","):
+            if not name or name == args.config:
+                continue
+            c = CONFIGS[name]
+            it2 = workload(c)
+            m2, b2 = time_layer(c, it2, max(10, min(args.steps, 40)), 3)
+            g2 = sum(b2) / (sum(m2) * 1e-3) / 1e9
+            per_config[name] = {"ms_per_step": round(statistics.mean(m2), 5), "weight_gbs": round(g2, 1),
+                                "roof_frac": round(g2 / peak, 4),
+                                "mean_active_experts": statistics.mean(i["G"] for i in it2),
+                                "rows": statistics.mean(i["R"] for i in it2)}
+    launches_per_step = 6
+    out = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "ms_per_step_median": round(statistics.median(ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
+        "data": "synthetic (seeded; NVFP4 codes drawn directly, bf16 activations N(0,1))",
+        "config": {
+            "workload": f"{cfg.name}: {cfg.E} experts, hidden {cfg.H}, intermediate {cfg.I}, "
+                        + (f"{cfg.T} token(s) top-{cfg.k}" if cfg.routing == "topk" else
+                           f"all experts, Mg~U{{{cfg.mg_lo}..{cfg.mg_hi}}}"),
+            "mean_active_experts": statistics.mean(i["G"] for i in items),
+            "rows_per_step": statistics.mean(i["R"] for i in items),
+            "bytes_per_step": statistics.mean(byts),
+            "l2": "flushed before every timed step (write of 2x L2); routing rotated over 20 seeded draws",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roof_frac": round(gbs / world / peak, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gemm_kernel (w13 grouped GEMM)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(),
+            "algorithmic_bytes_per_launch": round(w13_bytes),
+        },
+        "stage_ms": {k: round(v, 5) for k, v in stages.items()},
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(statistics.mean(e2e_ms), 5),
+                "h2d_bytes_per_step": round(h2d), "d2h_bytes_per_step": round(d2h)},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "per_config": per_config,
+        "device": props.name,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the reported baseline, and the reference arm)
+# ---------------------------------------------------------------------------
+
+ORACLE_SAMPLE_EXPERTS = 2
+
+
+def oracle_sample_step(cfg_name, seed_index=0):
+    """One oracle layer step on a bounded sample of the workload: the first
+    token of a seeded routing with its first ORACLE_SAMPLE_EXPERTS routed
+    slots kept (about a second of single-core work), host weights generated
+    for just the experts it reaches (renumbered). Returns (algorithmic bytes
+    of the sample, seconds, description)."""
+    import numpy as np
+    import torch
+
+    from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_activations, make_routing, make_weights
+    from oracle import nvfp4_moe as O
+
+    cfg = CONFIGS[cfg_name]
+    ids, tw = make_routing(cfg, seed=2 + 1000 * seed_index)
+    ntok = 1
+    ids, tw = ids[:ntok].clone(), tw[:ntok]
+    kept = 0
+    for j in range(ids.shape[1]):
+        if 0 <= int(ids[0, j]) < cfg.E and kept < ORACLE_SAMPLE_EXPERTS:
+            kept += 1
+        else:
+            ids[0, j] = -1
+    used = sorted(set(int(e) for e in ids.flatten().tolist() if 0 <= e < cfg.E))
+    remap = {e: i for i, e in enumerate(used)}
+    ids_c = torch.tensor([[remap.get(int(e), -1) for e in row] for row in ids.tolist()], dtype=torch.int32)
+    w = make_weights(len(used), cfg.H, cfg.I, seed=3 + seed_index)
+    w_np = {k: v.numpy() for k, v in w.items()}
+    x = make_activations(ntok, cfg.H, seed=1 + 1000 * seed_index)
+    x_bits = x.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    O.moe_layer(x_bits, ids_c.numpy(), tw.numpy(), w_np, E=len(used))
+    sec = time.perf_counter() - t0
+    desc = (f"{ntok} token of {cfg_name} routed to {len(used)} experts (its first {len(used)} of top-{cfg.k}), "
+            f"hidden {cfg.H}, intermediate {cfg.I}: one oracle layer step per sample, 1 thread")
+    return step_bytes(cfg, len(used), ntok), sec, desc
+
+
+def oracle_child(args):
+    """Runs in a child process with one BLAS/OpenMP thread."""
+    total_b, total_s, n, desc = 0, 0.0, 0, ""
+    t_start = time.time()
+    i = 0
+    while True:
+        b, s, desc = oracle_sample_step(args.config, i)
+        if i >= args.child_warmup:
+            total_b += b
+            total_s += s
+            n += 1
+        i += 1
+        if args.child_steps and n >= args.child_steps:
+            break
+        if not args.child_steps and time.time() - t_start > args.cpu_seconds and n >= 1:
+            break
+    print(json.dumps({"bytes": total_b, "seconds": total_s, "steps": n, "desc": desc}))
+
+
+def run_oracle_child(config, seconds, steps=0, warmup=0):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--config", config,
+           "--cpu-seconds", str(seconds), "--child-steps", str(steps), "--child-warmup", str(warmup)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(config, seconds):
+    res = run_oracle_child(config, seconds)
+    gbs = res["bytes"] / res["seconds"] / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{res['steps']} step(s): {res['desc']}", "ms_per_step": round(1e3 * res["seconds"] / res["steps"], 1),
+            "cpu_model": cpu_model()}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS
+    cfg = CONFIGS[args.config]
+    res = run_oracle_child(args.config, args.cpu_seconds, steps=args.steps, warmup=args.warmup)
+    gbs = res["bytes"] / res["seconds"] / 1e9
+    ms = 1e3 * res["seconds"] / res["steps"]
+    sample = f"{res['steps']} timed step(s) after {args.warmup} warm-up: {res['desc']}"
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle; fp32 codec divisions)",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {cfg.E} experts, hidden {cfg.H}, intermediate {cfg.I}",
+                   "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode_m1")
+    ap.add_argument("--extra", default="decode_m8,decode_m32",
+                    help="further configs timed on one GPU and reported under per_config")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="short run for ncu: warm-up and timed steps only")
+    ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling cases)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--child-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--child-warmup", type=int, default=0, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup) if not args.oracle_child else args.warmup
+    if args.oracle_child:
+        oracle_child(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_bench(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()
