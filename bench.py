@@ -238,11 +238,11 @@ def gpu_bench(args, rank, world):
             evs[1].record(stream)
             N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf)
             evs[2].record(stream)
-            N.nvfp4_grouped_gemm(xq, xsf, G1, W.w13_packed, W.w13_sf, d13)
+            N.nvfp4_grouped_gemm(xq, xsf, G1, W.w13, d13)
             evs[3].record(stream)
             N.swiglu_quantize_grouped(d13, G1, W.g_gate_up, hq, hsf)
             evs[4].record(stream)
-            N.nvfp4_grouped_gemm(hq, hsf, G1, W.w2_packed, W.w2_sf, d2)
+            N.nvfp4_grouped_gemm(hq, hsf, G1, W.w2, d2)
             evs[5].record(stream)
             N.moe_scatter_add(d2, it["ids"], it["tw"], c.E, G1, W.g_down, y)
             evs[6].record(stream)

@@ -82,17 +82,16 @@ typedef struct {
   int32_t* slot_row;
 } moe_groups_t;
 
-/* Expert weights (device). w13 rows 0..I-1 are gate, I..2I-1 are up, back to
- * back; w13_sf is gate's atom region followed by up's (first page, "The seam
- * CUTLASS forced open"; bit-identical to one region over 2I rows because
- * I % 128 == 0). */
+/* Expert weights (device), in the GEMM tiling made once at load time by
+ * nvfp4_tile_weights from packed e2m1 [E, N, K/2] and linear e4m3 scales
+ * [E, N, K/16]. w13 rows 0..I-1 are gate, I..2I-1 are up, back to back (first
+ * page, "The seam CUTLASS forced open": the pair doubles as the fused w13
+ * operand; with I % 128 == 0 no tile straddles the two halves). */
 typedef struct {
   int E;
-  const uint8_t* w13_packed;  /* [E, 2I, H/2] */
-  const uint8_t* w13_sf;      /* [E, 2I*H/16] atom layout, one region per expert */
+  const uint8_t* w13_tiled;   /* nvfp4_tiled_bytes(E*2I, H) bytes: w13 [E, 2I, H] */
   const float* g_gate_up;     /* [E, 2]: gate global, up global */
-  const uint8_t* w2_packed;   /* [E, H, I/2] */
-  const uint8_t* w2_sf;       /* [E, H*I/16] atom layout */
+  const uint8_t* w2_tiled;    /* nvfp4_tiled_bytes(E*H, I) bytes: w2 [E, H, I] */
   const float* g_down;        /* [E] */
 } moe_nvfp4_weights_t;
 
@@ -134,40 +133,41 @@ int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, in
 /* a3 / a6 -- nvfp4_quantize_rows: grouped bf16 rows [R_max, K] -> packed
  * [R_max, K/2] (rows >= R untouched) and the per-group padded scale region
  * `sf` (nvfp4_sf_bytes(R_max, E, K) bytes; padding bytes written as 0).
- * First page, "What changed" and "Proof" (byte-for-byte vs the host codec,
- * group_m = {1, 130}). K % 64 == 0. */
-int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, const moe_groups_t* groups,
+ * E is the expert count the groups were built for. First page, "What
+ * changed" and "Proof" (byte-for-byte vs the host codec, group_m = {1, 130}).
+ * K % 64 == 0. */
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups,
                         uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
 /* a2 + a3 fused: quantizes x[row_slot[r]/k, :] straight into grouped NVFP4
  * rows; output identical to moe_gather_rows followed by nvfp4_quantize_rows. */
-int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, const moe_groups_t* groups,
+int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups,
                              uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
 /* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
  * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
  * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
- * W is [E, N, K/2] packed with w_sf [E, N*K/16] in the atom layout. One
- * launch for all groups on tcgen05 block-scaled MMA (kind::mxf4nvf4, scale
- * vector 16), accumulators in tensor memory. First page, "What changed":
- * grouped GEMM w13 N=4096 K=4096 and w2 N=4096 K=2048, alpha = 1.
- * N % 128 == 0, K % 64 == 0. */
+ * W [E, N, K] comes tiled by nvfp4_tile_weights. One launch for all groups on
+ * tcgen05 block-scaled MMA (kind::mxf4nvf4, scale vector 16), accumulators in
+ * tensor memory. First page, "What changed": grouped GEMM w13 N=4096 K=4096
+ * and w2 N=4096 K=2048, alpha = 1. N % 128 == 0, K % 64 == 0; every pointer
+ * 16-byte aligned. */
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
-                       int R_max, const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K,
-                       float* d, cudaStream_t stream);
+                       int R_max, const uint8_t* w_tiled, int E, int N, int K, float* d,
+                       cudaStream_t stream);
 
 /* a5 -- swiglu_grouped: h[r, n] = silu(d13[r, n]*g_gate[e]) * (d13[r, I+n]*g_up[e]),
  * computed in fp32 (CUDA expf) and rounded once to bf16. d13 [R_max, 2I]
  * fp32, h [R_max, I] bf16. Second page, "Different globals on the two halves",
  * option (a): the per-half globals are applied here. */
-int swiglu_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups,
+int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups,
                    const float* g_gate_up, uint16_t* h, cudaStream_t stream);
 
 /* a5 + a6 fused: SwiGLU as swiglu_grouped, then the a3 codec on the bf16 h,
  * written as packed [R_max, I/2] + per-group padded scales
  * (nvfp4_sf_bytes(R_max, E, I) bytes). Identical to swiglu_grouped followed
  * by nvfp4_quantize_rows. */
-int swiglu_quantize_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups,
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups,
                             const float* g_gate_up, uint8_t* packed, uint8_t* sf,
                             cudaStream_t stream);
 
@@ -193,6 +193,21 @@ size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I);
 int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
                     const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
                     void* workspace, size_t ws_bytes, uint16_t* y, cudaStream_t stream);
+
+/* Load-time helper (not part of the timed step): weight tiling for the
+ * grouped GEMM. packed [rows, K/2] e2m1 and linear scales [rows, K/16] ->
+ * `tiled` (nvfp4_tiled_bytes(rows, K) bytes): for each 128-row tile and each
+ * 256-value K stage, 16 KB of packed bytes in the 128-byte-swizzled order the
+ * MMA reads from shared memory (16-byte chunk c of row r at chunk c ^ (r%8))
+ * followed by the stage's 2 KB of scales in the atom layout; values past K
+ * are zero. Same bytes as the inputs (up to the K padding), reordered so that
+ * each stage is one contiguous read. Like the first page's load-time scale
+ * swizzle ("The seam CUTLASS forced open"), it is paid once per weight, not
+ * per step. For stacked experts pass rows = E*N. rows % 128 == 0,
+ * K % 64 == 0. */
+size_t nvfp4_tiled_bytes(int rows, int K);
+int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
+                       cudaStream_t stream);
 
 /* Load-time helper (not part of the timed step): linear row-major scales
  * [N, K/16] -> the atom layout, N padded up to a multiple of 128 with zero

@@ -24,8 +24,8 @@ class MoeGroups(ctypes.Structure):
 
 
 class MoeWeights(ctypes.Structure):
-    _fields_ = [("E", c_int), ("w13_packed", c_void_p), ("w13_sf", c_void_p), ("g_gate_up", c_void_p),
-                ("w2_packed", c_void_p), ("w2_sf", c_void_p), ("g_down", c_void_p)]
+    _fields_ = [("E", c_int), ("w13_tiled", c_void_p), ("g_gate_up", c_void_p), ("w2_tiled", c_void_p),
+                ("g_down", c_void_p)]
 
 
 _SIGS = {
@@ -37,15 +37,15 @@ _SIGS = {
     "moe_route_groups": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p]),
     "moe_gather_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups),
                                 c_void_p, c_void_p]),
-    "nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
-                                    c_void_p]),
-    "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
-                                         c_void_p, c_void_p]),
-    "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_void_p,
-                                   c_int, c_int, c_int, c_void_p, c_void_p]),
-    "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
+    "nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
+                                    c_void_p, c_void_p]),
+    "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(MoeGroups),
+                                         c_void_p, c_void_p, c_void_p]),
+    "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int, c_int,
+                                   c_int, c_void_p, c_void_p]),
+    "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
                                c_void_p]),
-    "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
+    "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
                                         c_void_p, c_void_p, c_void_p]),
     "moe_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                 ctypes.POINTER(MoeGroups), c_void_p, c_void_p, c_void_p]),
@@ -53,6 +53,8 @@ _SIGS = {
     "moe_nvfp4_layer": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                 ctypes.POINTER(MoeWeights), c_void_p, c_size_t, c_void_p, c_void_p]),
     "nvfp4_swizzle_block_scales": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
+    "nvfp4_tiled_bytes": (c_size_t, [c_int, c_int]),
+    "nvfp4_tile_weights": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p]),
 }
 
 
@@ -151,37 +153,52 @@ def moe_gather_rows(x, topk_ids, E: int, groups: Groups, xg, stream=None):
 
 def nvfp4_quantize_rows(rows, groups: Groups, packed, sf, stream=None):
     R, K = rows.shape
-    _check("nvfp4_quantize_rows", load().nvfp4_quantize_rows(_ptr(rows), R, K, ctypes.byref(groups.struct),
-                                                             _ptr(packed), _ptr(sf), _stream(stream)))
+    _check("nvfp4_quantize_rows", load().nvfp4_quantize_rows(_ptr(rows), R, K, groups.E,
+                                                             ctypes.byref(groups.struct), _ptr(packed), _ptr(sf),
+                                                             _stream(stream)))
 
 
 def moe_gather_quantize_rows(x, k: int, groups: Groups, packed, sf, stream=None):
     T, H = x.shape
     _check("moe_gather_quantize_rows",
-           load().moe_gather_quantize_rows(_ptr(x), T, H, k, ctypes.byref(groups.struct), _ptr(packed), _ptr(sf),
-                                           _stream(stream)))
+           load().moe_gather_quantize_rows(_ptr(x), T, H, k, groups.E, ctypes.byref(groups.struct), _ptr(packed),
+                                           _ptr(sf), _stream(stream)))
 
 
-def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w_packed, w_sf, d, stream=None):
+class TiledWeight:
+    """One projection of all experts, [E, N, K], tiled for the grouped GEMM."""
+
+    def __init__(self, packed, sf_linear, stream=None):
+        import torch
+        self.E, self.N, K2 = packed.shape
+        self.K = 2 * K2
+        rows = self.E * self.N
+        self.data = torch.empty(load().nvfp4_tiled_bytes(rows, self.K), dtype=torch.uint8, device=packed.device)
+        _check("nvfp4_tile_weights",
+               load().nvfp4_tile_weights(_ptr(packed.contiguous()), _ptr(sf_linear.contiguous()), rows, self.K,
+                                         _ptr(self.data), _stream(stream)))
+
+
+def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w: TiledWeight, d, stream=None):
     R_max = a_packed.shape[0]
     K = a_packed.shape[1] * 2
-    E, N = w_packed.shape[0], w_packed.shape[1]
+    assert K == w.K
     _check("nvfp4_grouped_gemm",
-           load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max,
-                                     _ptr(w_packed), _ptr(w_sf), E, N, K, _ptr(d), _stream(stream)))
+           load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max, _ptr(w.data),
+                                     w.E, w.N, K, _ptr(d), _stream(stream)))
 
 
 def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):
     R_max, I2 = d13.shape
-    _check("swiglu_grouped", load().swiglu_grouped(_ptr(d13), R_max, I2 // 2, ctypes.byref(groups.struct),
+    _check("swiglu_grouped", load().swiglu_grouped(_ptr(d13), R_max, I2 // 2, groups.E, ctypes.byref(groups.struct),
                                                    _ptr(g_gate_up), _ptr(h), _stream(stream)))
 
 
 def swiglu_quantize_grouped(d13, groups: Groups, g_gate_up, packed, sf, stream=None):
     R_max, I2 = d13.shape
     _check("swiglu_quantize_grouped",
-           load().swiglu_quantize_grouped(_ptr(d13), R_max, I2 // 2, ctypes.byref(groups.struct), _ptr(g_gate_up),
-                                          _ptr(packed), _ptr(sf), _stream(stream)))
+           load().swiglu_quantize_grouped(_ptr(d13), R_max, I2 // 2, groups.E, ctypes.byref(groups.struct),
+                                          _ptr(g_gate_up), _ptr(packed), _ptr(sf), _stream(stream)))
 
 
 def moe_scatter_add(d2, topk_ids, topk_w, E: int, groups: Groups, g_down, y, stream=None):
@@ -206,29 +223,24 @@ def moe_nvfp4_layer_workspace_size(T: int, k: int, E: int, H: int, I: int) -> in
 class Weights:
     """Device NVFP4 expert weights in the layout moe_nvfp4_layer reads.
 
-    Built from packed nibbles, LINEAR block scales and globals; the scales are
-    swizzled into the atom layout once here (load time, on the GPU)."""
+    Built from packed nibbles, LINEAR block scales and globals; both
+    projections are tiled for the grouped GEMM once here (load time, on the
+    GPU). The inputs are not kept."""
 
     def __init__(self, w13_packed, w13_sf_linear, g_gate_up, w2_packed, w2_sf_linear, g_down, stream=None):
         import torch
         self.E, I2, H2 = w13_packed.shape
         self.H, self.I = H2 * 2, I2 // 2
-        self.w13_packed = w13_packed.contiguous()
-        self.w2_packed = w2_packed.contiguous()
+        self.w13 = TiledWeight(w13_packed, w13_sf_linear, stream)
+        self.w2 = TiledWeight(w2_packed, w2_sf_linear, stream)
         self.g_gate_up = g_gate_up.to(torch.float32).contiguous()
         self.g_down = g_down.to(torch.float32).contiguous()
-        dev = w13_packed.device
-        self.w13_sf = torch.empty((self.E, 2 * self.I * self.H // 16), dtype=torch.uint8, device=dev)
-        self.w2_sf = torch.empty((self.E, self.H * self.I // 16), dtype=torch.uint8, device=dev)
-        nvfp4_swizzle_block_scales(w13_sf_linear.reshape(-1, self.H // 16).contiguous(), self.w13_sf, stream)
-        nvfp4_swizzle_block_scales(w2_sf_linear.reshape(-1, self.I // 16).contiguous(), self.w2_sf, stream)
-        self.struct = MoeWeights(self.E, self.w13_packed.data_ptr(), self.w13_sf.data_ptr(),
-                                 self.g_gate_up.data_ptr(), self.w2_packed.data_ptr(), self.w2_sf.data_ptr(),
-                                 self.g_down.data_ptr())
+        self.struct = MoeWeights(self.E, self.w13.data.data_ptr(), self.g_gate_up.data_ptr(),
+                                 self.w2.data.data_ptr(), self.g_down.data_ptr())
 
     @property
     def nbytes(self) -> int:
-        return sum(t.numel() for t in (self.w13_packed, self.w13_sf, self.w2_packed, self.w2_sf))
+        return self.w13.data.numel() + self.w2.data.numel()
 
 
 def moe_nvfp4_layer(x, topk_ids, topk_w, weights: Weights, workspace, y, stream=None):
@@ -247,7 +259,7 @@ class MoeLayer:
         import torch
         self.weights, self.k, self.T_max = weights, k, T_max
         n = moe_nvfp4_layer_workspace_size(T_max, k, weights.E, weights.H, weights.I)
-        self.workspace = torch.empty(n, dtype=torch.uint8, device=weights.w13_packed.device)
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=weights.w13.data.device)
 
     def __call__(self, x, topk_ids, topk_w, y=None, stream=None):
         import torch

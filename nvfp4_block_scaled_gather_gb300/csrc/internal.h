@@ -26,12 +26,17 @@ cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g,
                           uint16_t* xg, cudaStream_t s);
 // src_k > 0: rows are x[row_slot[r] / src_k]; src_k == 0: rows are src[r].
-cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int K,
+// E bounds the group count (grid size); CTAs past the routed blocks exit.
+cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
                             const moe_groups_t& g, uint8_t* packed, uint8_t* sf, cudaStream_t s);
 // h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
-cudaError_t launch_swiglu(const float* d13, int R_max, int I, const moe_groups_t& g,
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g,
                           const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf,
                           cudaStream_t s);
+// Load-time weight tiling for the grouped GEMM (rows % 128 == 0).
+cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
+                        cudaStream_t s);
+inline size_t tiled_bytes(long long rows, long long K) { return (size_t)(rows / 128) * ((K + 255) / 256) * 18432; }
 cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w,
                            int T, int k, int E, const moe_groups_t& g, const float* g_down,
                            uint16_t* y, cudaStream_t s);
@@ -39,8 +44,7 @@ cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzle
 
 // tcgen05 grouped GEMM (nvfp4_gemm.cu). status: device word for wait timeouts.
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf,
-                                const moe_groups_t& g, int R_max, const uint8_t* w_packed,
-                                const uint8_t* w_sf, int E, int N, int K, float* d, int* status,
-                                cudaStream_t s);
+                                const moe_groups_t& g, int R_max, const uint8_t* w_tiled, int E, int N,
+                                int K, float* d, int* status, cudaStream_t s);
 
 }  // namespace moe

@@ -162,56 +162,56 @@ int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, in
   return status_of(launch_gather(x, H, k, T * k, *groups, xg, stream));
 }
 
-int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, const moe_groups_t* groups, uint8_t* packed,
-                        uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || K <= 0) return MOE_ERR_INVALID;
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups,
+                        uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || K <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID;
   if (K % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!rows || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_quantize(rows, 0, R_max, K, *groups, packed, sf, stream));
+  return status_of(launch_quantize(rows, 0, R_max, E, K, *groups, packed, sf, stream));
 }
 
-int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, const moe_groups_t* groups, uint8_t* packed,
-                             uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0) return MOE_ERR_INVALID;
+int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups,
+                             uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || E <= 0 || E > kMaxExperts)
+    return MOE_ERR_INVALID;
   if (H % 64) return MOE_ERR_SHAPE;
   if (T * k == 0) return MOE_OK;
   if (!x || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_quantize(x, k, T * k, H, *groups, packed, sf, stream));
+  return status_of(launch_quantize(x, k, T * k, E, H, *groups, packed, sf, stream));
 }
 
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
-                       const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K, float* d,
-                       cudaStream_t stream) {
+                       const uint8_t* w_tiled, int E, int N, int K, float* d, cudaStream_t stream) {
   if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID;
   if (N % 128 || K % 64) return MOE_ERR_SHAPE;
   if ((long long)E * N > (1LL << 31)) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
-  if (!a_packed || !a_sf || !w_packed || !w_sf || !d) return MOE_ERR_INVALID;
-  if (reinterpret_cast<uintptr_t>(a_packed) % 16 || reinterpret_cast<uintptr_t>(w_packed) % 16 ||
-      reinterpret_cast<uintptr_t>(a_sf) % 16 || reinterpret_cast<uintptr_t>(w_sf) % 16)
+  if (!a_packed || !a_sf || !w_tiled || !d) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(a_packed) % 16 || reinterpret_cast<uintptr_t>(w_tiled) % 16 ||
+      reinterpret_cast<uintptr_t>(a_sf) % 16)
     return MOE_ERR_INVALID;
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_packed, w_sf, E, N, K, d, st, stream));
+  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, st, stream));
 }
 
-int swiglu_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups, const float* g_gate_up,
+int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
                    uint16_t* h, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || I <= 0) return MOE_ERR_INVALID;
+  if (!groups_ok(groups) || R_max < 0 || I <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID;
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, I, *groups, g_gate_up, h, nullptr, nullptr, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, g_gate_up, h, nullptr, nullptr, stream));
 }
 
-int swiglu_quantize_grouped(const float* d13, int R_max, int I, const moe_groups_t* groups, const float* g_gate_up,
-                            uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || I <= 0) return MOE_ERR_INVALID;
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups,
+                            const float* g_gate_up, uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || I <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID;
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, I, *groups, g_gate_up, nullptr, packed, sf, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, g_gate_up, nullptr, packed, sf, stream));
 }
 
 int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k, int E,
@@ -237,7 +237,8 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (H % 128 || I % 128) return MOE_ERR_SHAPE;
   if (T == 0) return MOE_OK;
   if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
-  if (!w->w13_packed || !w->w13_sf || !w->g_gate_up || !w->w2_packed || !w->w2_sf || !w->g_down)
+  if (!w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !w->g_down) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(w->w13_tiled) % 16 || reinterpret_cast<uintptr_t>(w->w2_tiled) % 16)
     return MOE_ERR_INVALID;
   if ((long long)T * k > (1LL << 30) || (long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
   if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
@@ -249,14 +250,32 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (!st) return MOE_ERR_CUDA;
   const int S = T * k;
   cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
-  if (err == cudaSuccess) err = launch_quantize(x, k, S, H, ws.groups, ws.xq, ws.xsf, stream);
+  if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, ws.xq, ws.xsf, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_packed, w->w13_sf, E, 2 * I, H, ws.d13, st, stream);
-  if (err == cudaSuccess) err = launch_swiglu(ws.d13, S, I, ws.groups, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
+    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, st, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_packed, w->w2_sf, E, H, I, ws.d2, st, stream);
+    err = launch_swiglu(ws.d13, S, E, I, ws.groups, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
+  if (err == cudaSuccess)
+    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, st, stream);
   if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
+}
+
+size_t nvfp4_tiled_bytes(int rows, int K) {
+  if (rows < 0 || K <= 0) return 0;
+  return tiled_bytes(rows, K);
+}
+
+int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
+                       cudaStream_t stream) {
+  if (rows < 0 || K <= 0) return MOE_ERR_INVALID;
+  if (rows % 128 || K % 64) return MOE_ERR_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!packed || !sf_linear || !tiled) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(packed) % 16 || reinterpret_cast<uintptr_t>(sf_linear) % 4 ||
+      reinterpret_cast<uintptr_t>(tiled) % 16)
+    return MOE_ERR_INVALID;
+  return status_of(launch_tile(packed, sf_linear, rows, K, tiled, stream));
 }
 
 int nvfp4_swizzle_block_scales(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t stream) {

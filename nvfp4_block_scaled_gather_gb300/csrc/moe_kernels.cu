@@ -157,129 +157,155 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
   }
 }
 
-// Loads 64 bf16 (128 bytes) as fp32.
-__device__ __forceinline__ void load64_bf16(const uint16_t* __restrict__ p, float* v) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
+// Four lanes (4j .. 4j+3 of a warp) hold one 16-value block, four values
+// each; sixteen lanes hold the four blocks of one 4-byte scale word. Each lane
+// writes its two packed bytes; the first lane of each 16 writes the word.
+// Lanes that are not `active` compute along (shuffles need the full warp) but
+// write nothing; a 16-lane group is either wholly active or wholly not.
+__device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool active, int lane,
+                                                    uint8_t* __restrict__ packed_dst, uint8_t* __restrict__ sf_blk,
+                                                    int m, int c, int Kc) {
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
+  const uint32_t s = e4m3_encode(__fdiv_rn(amax, 6.0f));
+  const float d = e4m3_decode(s);
+  uint32_t codes = 0u;
+  if (d != 0.0f) {  // an underflowed block keeps all-zero codes
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 u = __ldg(q + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
-      v[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
-    }
+    for (int i = 0; i < 4; ++i) codes |= e2m1_encode(__fdiv_rn(v[i], d)) << (4 * i);
   }
+  const uint32_t s1 = __shfl_down_sync(~0u, s, 4), s2 = __shfl_down_sync(~0u, s, 8),
+                 s3 = __shfl_down_sync(~0u, s, 12);
+  if (!active) return;
+  *reinterpret_cast<uint16_t*>(packed_dst) = (uint16_t)codes;
+  if ((lane & 15) == 0)
+    *reinterpret_cast<uint32_t*>(sf_blk + sf_atom_offset(m, c, Kc)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
-// Quantizes 64 values (4 blocks): 32 packed bytes and 4 scale bytes.
-__device__ __forceinline__ void quantize64_store(const float* v, uint8_t* __restrict__ packed_dst,
-                                                 uint32_t* __restrict__ sf_word) {
-  uint32_t words[8], scales = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const Nvfp4Block q = quantize16(v + 16 * b);
-    words[2 * b] = q.lo;
-    words[2 * b + 1] = q.hi;
-    scales |= q.scale << (8 * b);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(packed_dst);
-  dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-  dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-  *sf_word = scales;
-}
+// The CTA's 128-row scale block `blk`: first grouped row, valid rows and group.
+struct RowBlock {
+  int row0, nvalid, gi;
+};
 
-// ---------------------------------------------------------------------------
-// a3 / a6 quantize (with optional a2 gather). Work item = (scale row rho of
-// the padded per-group region, 64-column chunk j). Real rows are quantized;
-// padding rows get zero scale words.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k,
-                                                            int K, moe_groups_t g, uint8_t* __restrict__ packed,
-                                                            uint8_t* __restrict__ sf) {
-  const int G = __ldg(g.counts + 0);
-  const int nblk = __ldg(g.counts + 3);
-  const int chunks = K / 64, Kc = K / 16;
-  const long long total = (long long)nblk * 128 * chunks;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int rho = (int)(i / chunks), j = (int)(i % chunks);
-    const int blk = rho >> 7;
+__device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int blk) {
+  __shared__ int s_info[3];
+  if (threadIdx.x == 0) {
+    const int G = __ldg(g.counts + 0);
     const int gi = find_group(g.group_sf_block, G, blk);
-    const int gblk = __ldg(g.group_sf_block + gi);
-    const int m = (blk - gblk) * 128 + (rho & 127);
+    const int m0 = (blk - __ldg(g.group_sf_block + gi)) * 128;
     const int r0 = __ldg(g.group_offsets + gi);
     const int mg = __ldg(g.group_offsets + gi + 1) - r0;
-    uint32_t* word = reinterpret_cast<uint32_t*>(sf + (size_t)gblk * 128 * Kc + sf_atom_offset(m, 4 * j, Kc));
-    if (m >= mg) { *word = 0u; continue; }
-    const int r = r0 + m;
-    const int srow = src_k > 0 ? __ldg(g.row_slot + r) / src_k : r;
-    float v[64];
-    load64_bf16(src + (size_t)srow * K + 64 * j, v);
-    quantize64_store(v, packed + (size_t)r * (K / 2) + 32 * j, word);
+    s_info[0] = r0 + m0;
+    s_info[1] = min(128, mg - m0);
+    s_info[2] = gi;
+  }
+  __syncthreads();
+  return RowBlock{s_info[0], s_info[1], s_info[2]};
+}
+
+// Zeroes the scale words of padding rows (>= nvalid) of a block's atoms
+// [a0, a0 + na); real rows' words are written by the quantizing lanes.
+__device__ __forceinline__ void zero_padding_words(uint8_t* __restrict__ sf_blk, int a0, int na, int nvalid) {
+  uint32_t* words = reinterpret_cast<uint32_t*>(sf_blk + (size_t)a0 * 512);
+  for (int w = threadIdx.x; w < na * 128; w += blockDim.x) {
+    const int wi = w & 127;                    // word wi of an atom holds row (wi/4) + 32*(wi%4)
+    if ((wi >> 2) + 32 * (wi & 3) >= nvalid) words[w] = 0u;
   }
 }
 
+constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K)
+
 // ---------------------------------------------------------------------------
-// a5 (+ a6) SwiGLU with per-group gate/up globals. Same work items as the
-// quantizer over an I-wide operand; each item reads 64 gate and 64 up fp32.
+// a3 / a6 quantize (with optional a2 gather). Grid: (128-row scale block,
+// 1024-value column chunk); CTAs past the routed block count exit. Each lane
+// quantizes 4 values; padding rows of the block get zero scale words.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k, int K,
+                                                            moe_groups_t g, uint8_t* __restrict__ packed,
+                                                            uint8_t* __restrict__ sf) {
+  const int blk = blockIdx.x;
+  if (blk >= __ldg(g.counts + 3)) return;
+  const RowBlock rb = resolve_block(g, blk);
+  const int Kc = K / 16;
+  const int kc0 = blockIdx.y * kColsPerCta;
+  const int kcount = min(kColsPerCta, K - kc0);
+  const int quads = kcount / 4;
+  const int total = rb.nvalid * quads;
+  const int lane = threadIdx.x & 31;
+  uint8_t* sf_blk = sf + (size_t)blk * 128 * Kc;
+  for (int base = (threadIdx.x & ~31); base < total; base += blockDim.x) {
+    const int item = base + lane;
+    const bool active = item < total;
+    const int m = active ? item / quads : 0;
+    const int q = active ? item - m * quads : 0;
+    const int r = rb.row0 + m;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      const int srow = src_k > 0 ? __ldg(g.row_slot + r) / src_k : r;
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)srow * K + kc0 + 4 * q));
+      v[0] = bf16_to_f32(u.x & 0xFFFFu);
+      v[1] = bf16_to_f32(u.x >> 16);
+      v[2] = bf16_to_f32(u.y & 0xFFFFu);
+      v[3] = bf16_to_f32(u.y >> 16);
+    }
+    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2, sf_blk, m,
+                        (kc0 + 4 * q) / 16, Kc);
+  }
+  zero_padding_words(sf_blk, kc0 / 64, kcount / 64, rb.nvalid);
+}
+
+// ---------------------------------------------------------------------------
+// a5 (+ a6) SwiGLU with per-group gate/up globals; same grid as the quantizer
+// over the I-wide output. Each lane reads 4 gate and 4 up fp32 values.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int I, moe_groups_t g,
                                                           const float* __restrict__ g_gate_up,
                                                           uint16_t* __restrict__ h, uint8_t* __restrict__ packed,
                                                           uint8_t* __restrict__ sf) {
-  const int G = __ldg(g.counts + 0);
-  const int nblk = __ldg(g.counts + 3);
-  const int chunks = I / 64, Kc = I / 16;
-  const long long total = (long long)nblk * 128 * chunks;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int rho = (int)(i / chunks), j = (int)(i % chunks);
-    const int blk = rho >> 7;
-    const int gi = find_group(g.group_sf_block, G, blk);
-    const int gblk = __ldg(g.group_sf_block + gi);
-    const int m = (blk - gblk) * 128 + (rho & 127);
-    const int r0 = __ldg(g.group_offsets + gi);
-    const int mg = __ldg(g.group_offsets + gi + 1) - r0;
-    uint32_t* word = h ? nullptr
-                       : reinterpret_cast<uint32_t*>(sf + (size_t)gblk * 128 * Kc + sf_atom_offset(m, 4 * j, Kc));
-    if (m >= mg) {
-      if (word) *word = 0u;
-      continue;
-    }
-    const int r = r0 + m;
-    const int e = __ldg(g.group_expert + gi);
-    const float gg = __ldg(g_gate_up + 2 * e), gu = __ldg(g_gate_up + 2 * e + 1);
-    const float4* gate = reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + 64 * j);
-    const float4* up = reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + I + 64 * j);
-    float v[64];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 a = __ldg(gate + q), b = __ldg(up + q);
+  const int blk = blockIdx.x;
+  if (blk >= __ldg(g.counts + 3)) return;
+  const RowBlock rb = resolve_block(g, blk);
+  const int e = __ldg(g.group_expert + rb.gi);
+  const float gg = __ldg(g_gate_up + 2 * e), gu = __ldg(g_gate_up + 2 * e + 1);
+  const int Kc = I / 16;
+  const int kc0 = blockIdx.y * kColsPerCta;
+  const int kcount = min(kColsPerCta, I - kc0);
+  const int quads = kcount / 4;
+  const int total = rb.nvalid * quads;
+  const int lane = threadIdx.x & 31;
+  uint8_t* sf_blk = h ? nullptr : sf + (size_t)blk * 128 * Kc;
+  for (int base = (threadIdx.x & ~31); base < total; base += blockDim.x) {
+    const int item = base + lane;
+    const bool active = item < total;
+    const int m = active ? item / quads : 0;
+    const int q = active ? item - m * quads : 0;
+    const int r = rb.row0 + m;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + kc0 + 4 * q));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + I + kc0 + 4 * q));
       const float ga[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int z = 0; z < 4; ++z) {
         const float gt = ga[z] * gg;
         const float u = ub[z] * gu;
         const float hv = gt / (1.0f + expf(-gt)) * u;
-        v[4 * q + z] = __uint_as_float(
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hv))) << 16);  // h rounded once to bf16
+        v[z] = bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));  // h rounded once to bf16
       }
     }
     if (h) {
-      uint4* dst = reinterpret_cast<uint4*>(h + (size_t)r * I + 64 * j);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int z = 0; z < 4; ++z)
-          w4[z] = (__float_as_uint(v[8 * q + 2 * z]) >> 16) | (__float_as_uint(v[8 * q + 2 * z + 1]) & 0xFFFF0000u);
-        dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      if (active) {
+        const uint32_t lo = (__float_as_uint(v[0]) >> 16) | (__float_as_uint(v[1]) & 0xFFFF0000u);
+        const uint32_t hi = (__float_as_uint(v[2]) >> 16) | (__float_as_uint(v[3]) & 0xFFFF0000u);
+        *reinterpret_cast<uint2*>(h + (size_t)r * I + kc0 + 4 * q) = make_uint2(lo, hi);
       }
     } else {
-      quantize64_store(v, packed + (size_t)r * (I / 2) + 32 * j, word);
+      quantize_quad_store(v, active, lane, packed + (size_t)r * (I / 2) + (kc0 + 4 * q) / 2, sf_blk, m,
+                          (kc0 + 4 * q) / 16, Kc);
     }
   }
+  if (!h) zero_padding_words(sf_blk, kc0 / 64, kcount / 64, rb.nvalid);
 }
 
 // ---------------------------------------------------------------------------
@@ -351,6 +377,43 @@ __global__ void __launch_bounds__(kThreads) swizzle_kernel(const uint8_t* __rest
   }
 }
 
+// ---------------------------------------------------------------------------
+// Load-time tiling of weights for the grouped GEMM: for every 128-row tile t
+// and 256-value K stage ks, an 18 KB block = 16 KB of e2m1 bytes in the
+// 128-byte-swizzled shared-memory image (16-byte chunk c of row r stored at
+// chunk c ^ (r % 8)) followed by the stage's four 512-byte scale atoms.
+// Values past K are zero.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restrict__ packed,
+                                                        const uint8_t* __restrict__ sf_linear, int tiles, int K,
+                                                        uint8_t* __restrict__ out) {
+  const int nk = (K + 255) / 256, rowb = K / 2, Kc = K / 16;
+  const long long chunks = (long long)tiles * nk * 128 * 8;
+  const long long words = (long long)tiles * nk * 4 * 128;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks + words;
+       i += (long long)gridDim.x * blockDim.x) {
+    if (i < chunks) {
+      const int c = (int)(i & 7), r = (int)((i >> 3) & 127);
+      const long long ts = i >> 10;  // t * nk + ks
+      const int ks = (int)(ts % nk), t = (int)(ts / nk);
+      const int col = ks * 128 + c * 16;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (col < rowb) v = __ldg(reinterpret_cast<const uint4*>(packed + ((size_t)t * 128 + r) * rowb + col));
+      *reinterpret_cast<uint4*>(out + (size_t)ts * 18432 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    } else {
+      const long long j = i - chunks;
+      const int wi = (int)(j & 127), a = (int)((j >> 7) & 3);
+      const long long ts = j >> 9;
+      const int ks = (int)(ts % nk), t = (int)(ts / nk);
+      const int m = (wi >> 2) + 32 * (wi & 3);
+      const int col = (4 * ks + a) * 4;  // first scale column of this atom
+      uint32_t v = 0u;
+      if (col < Kc) v = __ldg(reinterpret_cast<const uint32_t*>(sf_linear + ((size_t)t * 128 + m) * Kc + col));
+      *reinterpret_cast<uint32_t*>(out + (size_t)ts * 18432 + 16384 + a * 512 + wi * 4) = v;
+    }
+  }
+}
+
 int grid_for(long long items) {
   const long long need = (items + kThreads - 1) / kThreads;
   const long long cap = (long long)num_sms() * 16;
@@ -375,17 +438,25 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int K, const moe_groups_t& g,
+cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K, const moe_groups_t& g,
                             uint8_t* packed, uint8_t* sf, cudaStream_t s) {
-  const long long items = sf_blocks_bound(R_max, R_max) * 128 * (K / 64);
-  quantize_kernel<<<grid_for(items), kThreads, 0, s>>>(src, src_k, K, g, packed, sf);
+  const dim3 grid((unsigned)sf_blocks_bound(R_max, E), (K + kColsPerCta - 1) / kColsPerCta);
+  quantize_kernel<<<grid, kThreads, 0, s>>>(src, src_k, K, g, packed, sf);
   return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu(const float* d13, int R_max, int I, const moe_groups_t& g, const float* g_gate_up,
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, const float* g_gate_up,
                           uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
-  const long long items = sf_blocks_bound(R_max, R_max) * 128 * (I / 64);
-  swiglu_kernel<<<grid_for(items), kThreads, 0, s>>>(d13, I, g, g_gate_up, h, packed, sf);
+  const dim3 grid((unsigned)sf_blocks_bound(R_max, E), (I + kColsPerCta - 1) / kColsPerCta);
+  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, I, g, g_gate_up, h, packed, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
+                        cudaStream_t s) {
+  const long long tiles = rows / 128, nk = (K + 255) / 256;
+  const long long items = tiles * nk * (128 * 8 + 4 * 128);
+  tile_kernel<<<grid_for(items), kThreads, 0, s>>>(packed, sf_linear, (int)tiles, K, tiled);
   return cudaGetLastError();
 }
 

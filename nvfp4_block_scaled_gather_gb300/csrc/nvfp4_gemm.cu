@@ -15,8 +15,15 @@
 //  * Persistent CTAs (one per SM) walk the ragged work list of
 //    (128-row activation block, 128-row weight tile) units in a fixed order;
 //    every unit streams its weight tile over the full K once.
-//  * Warp roles: warp 0 issues TMA (weights and activations, 128B-swizzled)
-//    plus bulk copies of the e4m3 scale atoms into an mbarrier ring; warp 1
+//  * Weights arrive pre-tiled (nvfp4_tile_weights, a load-time step): for
+//    every 128-row tile and 256-value K stage, 16 KB of e2m1 bytes already in
+//    the 128-byte-swizzled shared-memory image followed by the 2 KB of e4m3
+//    scale atoms. A stage is one contiguous 18 KB bulk copy, so each CTA
+//    streams its tile's weights sequentially from HBM (row-major tiles read
+//    128 bytes from each of 128 rows 2 KB apart, which left DRAM half idle).
+//  * Warp roles: warp 0 issues the weight bulk copies (L2 evict-first), a TMA
+//    load of the token rows (128B-swizzled) and a bulk copy of their scale
+//    atoms into an mbarrier ring; warp 1
 //    copies scales into tensor memory (tcgen05.cp) and issues
 //    tcgen05.mma.kind::mxf4nvf4 (scale vector 16) into a double-buffered
 //    TMEM accumulator; warps 2-5 drain TMEM (tcgen05.ld) to fp32 global.
@@ -40,6 +47,7 @@ constexpr int kStageKBytes = 128;   // K bytes per stage and row = 256 e2m1 valu
 constexpr int kAtomBytes = 512;     // one scale atom: 128 rows x 4 scales (64 K values)
 constexpr int kATileBytes = kBM * kStageKBytes;  // 16 KB
 constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
+constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
 constexpr int kBBoxRows = 16;
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
@@ -48,7 +56,7 @@ constexpr int kTmemCols = 512;
 
 struct GemmArgs {
   const uint8_t* a_sf;
-  const uint8_t* w_sf;
+  const uint8_t* w_tiled;
   float* d;
   const int32_t* counts;
   const int32_t* group_offsets;
@@ -93,6 +101,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+// Bulk copy with an L2 policy (weights are read once per step: evict first).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -171,11 +193,11 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
 // One unit of work: 128-row activation block `chunk` (a group's rows
 // [128q, 128q + 128)) against 128-row weight tile `nt` of the group's expert.
 struct Unit {
-  int row0, nvalid, nmma, a_row, nt;
-  size_t sfa_off, sfb_off;
+  int row0, nvalid, nmma, nt;
+  size_t w_off, sfb_off;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int G, int kc4) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int G, int kc4, int nk) {
   const int chunk = u / n_tiles;
   Unit un;
   un.nt = u - chunk * n_tiles;
@@ -187,14 +209,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tile
   un.row0 = r0 + kBM * q;
   un.nvalid = min(kBM, mg - kBM * q);
   un.nmma = (un.nvalid + 15) & ~15;
-  un.a_row = e * p.N + un.nt * kBM;
-  un.sfa_off = ((size_t)e * n_tiles + un.nt) * kc4 * kAtomBytes;
+  un.w_off = ((size_t)e * n_tiles + un.nt) * nk * kWStageBytes;
   un.sfb_off = (size_t)chunk * kc4 * kAtomBytes;
   return un;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -220,14 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = (p.K + 255) / 256;       // stages per unit
   const int tn = min(kBM, max(16, (maxmg + 15) & ~15));   // token rows per B stage
   const int acc_cols = max(32, tn);
-  const int stage_bytes = kATileBytes + tn * kStageKBytes + 2 * kSfStageBytes;
+  const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
   const int avail = kSmemBytes - 1024 - 1024;
   int stages = min(kMaxStages, avail / stage_bytes);
   stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
-  const uint32_t sA = smem_u32(smem + 1024);
-  const uint32_t sB = sA + (uint32_t)stages * kATileBytes;
-  const uint32_t sSFA = sB + (uint32_t)stages * tn * kStageKBytes;
-  const uint32_t sSFB = sSFA + (uint32_t)stages * kSfStageBytes;
+  // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, then token scales
+  const uint32_t sW = smem_u32(smem + 1024);
+  const uint32_t sB = sW + (uint32_t)stages * kWStageBytes;
+  const uint32_t sSFB = sB + (uint32_t)stages * tn * kStageKBytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
@@ -261,21 +282,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
+      const uint64_t stream_policy = policy_evict_first();
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+        const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
         const int nbox = un.nmma / kBBoxRows;
         for (int ks = 0; ks < nk; ++ks) {
           if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
           const int natoms = min(4, kc4 - 4 * ks);
-          const uint32_t bytes = kATileBytes + nbox * kBBoxRows * kStageKBytes + 2u * natoms * kAtomBytes;
+          const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
+          const uint32_t bytes = wbytes + nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
           const uint32_t fb = full_bar(stage);
           mbar_expect_tx(fb, bytes);
-          tma_load_2d(sA + stage * kATileBytes, &tmA, ks * kStageKBytes, un.a_row, fb);
+          bulk_load_hint(sW + stage * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes, fb,
+                         stream_policy);
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, &tmB, ks * kStageKBytes,
                         un.row0 + b * kBBoxRows, fb);
-          bulk_load(sSFA + stage * kSfStageBytes, p.w_sf + un.sfa_off + (size_t)ks * kSfStageBytes,
-                    natoms * kAtomBytes, fb);
           bulk_load(sSFB + stage * kSfStageBytes, p.a_sf + un.sfb_off + (size_t)ks * kSfStageBytes,
                     natoms * kAtomBytes, fb);
           filled |= 1u << stage;
@@ -300,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+        const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
         if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
@@ -310,12 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+          const uint32_t sWs = sW + stage * kWStageBytes;
           for (int a = 0; a < natoms; ++a) {
-            tc_cp_scales(sf_col + 4 * a, desc_scales(sSFA + stage * kSfStageBytes + a * kAtomBytes));
+            tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
             tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
           }
           for (int a = 0; a < natoms; ++a) {
-            const uint64_t adesc = desc_sw128(sA + stage * kATileBytes + 32 * a);
+            const uint64_t adesc = desc_sw128(sWs + 32 * a);
             const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
             tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
           }
@@ -341,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const Unit un = decode_unit(u, p, n_tiles, G, kc4);
+      const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
       if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
       tc_fence_after();
       const int n = un.nt * kBM + quad * 32 + lane;
@@ -400,14 +423,12 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
-                                const uint8_t* w_packed, const uint8_t* w_sf, int E, int N, int K, float* d,
-                                int* status, cudaStream_t s) {
-  CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, w_packed, (uint64_t)K / 2, (uint64_t)E * N, kBM)) return cudaErrorInvalidValue;
+                                const uint8_t* w_tiled, int E, int N, int K, float* d, int* status, cudaStream_t s) {
+  CUtensorMap tmB;
   if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
   GemmArgs p;
   p.a_sf = a_sf;
-  p.w_sf = w_sf;
+  p.w_tiled = w_tiled;
   p.d = d;
   p.counts = g.counts;
   p.group_offsets = g.group_offsets;
@@ -421,7 +442,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
   if (err != cudaSuccess) return err;
   const long long units_bound = sf_blocks_bound(R_max, E < R_max ? E : R_max) * (N / kBM);
   const int grid = (int)(units_bound < num_sms() ? units_bound : num_sms());
-  gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+  gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmB, p);
   return cudaGetLastError();
 }
 

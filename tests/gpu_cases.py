@@ -61,14 +61,14 @@ def run_stages(x, ids, tw, W: N.Weights, E: int) -> dict:
     xsf = torch.zeros(N.sf_bytes(S, E, H), dtype=torch.uint8, device=dev)
     N.nvfp4_quantize_rows(xg, G, xq, xsf)
     d13 = torch.zeros(S, 2 * I, dtype=torch.float32, device=dev)
-    N.nvfp4_grouped_gemm(xq, xsf, G, W.w13_packed, W.w13_sf, d13)
+    N.nvfp4_grouped_gemm(xq, xsf, G, W.w13, d13)
     h = torch.zeros(S, I, dtype=torch.bfloat16, device=dev)
     N.swiglu_grouped(d13, G, W.g_gate_up, h)
     hq = torch.zeros(S, I // 2, dtype=torch.uint8, device=dev)
     hsf = torch.zeros(N.sf_bytes(S, E, I), dtype=torch.uint8, device=dev)
     N.nvfp4_quantize_rows(h, G, hq, hsf)
     d2 = torch.zeros(S, H, dtype=torch.float32, device=dev)
-    N.nvfp4_grouped_gemm(hq, hsf, G, W.w2_packed, W.w2_sf, d2)
+    N.nvfp4_grouped_gemm(hq, hsf, G, W.w2, d2)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     N.moe_scatter_add(d2, ids, tw, E, G, W.g_down, y)
     torch.cuda.synchronize()

@@ -52,15 +52,19 @@ def test_host_side_validation(native):
     g = _fake_groups()
     s = None
     # unsupported GEMM shapes
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 16, 4, 100, 256, 16, s) == 2
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 16, 4, 128, 96, 16, s) == 2
-    # missing group arrays / bad sizes
-    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 16, 4, 128, 256, 16, s) == 1
-    assert native.nvfp4_quantize_rows(16, 8, 100, ctypes.byref(g), 16, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 4, 100, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 4, 128, 96, 16, s) == 2
+    # missing group arrays / bad sizes / misaligned weights
+    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 24, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_quantize_rows(16, 8, 100, 4, ctypes.byref(g), 16, 16, s) == 2
+    assert native.nvfp4_quantize_rows(16, 8, 128, 0, ctypes.byref(g), 16, 16, s) == 1
+    assert native.nvfp4_tile_weights(16, 16, 100, 128, 16, s) == 2
+    assert native.nvfp4_tile_weights(16, 16, 128, 96, 16, s) == 2
     assert native.moe_route_groups(16, 2, 2, 2000, ctypes.byref(g), s) == 1
     assert native.moe_route_groups(16, 2, 40, 8, ctypes.byref(g), s) == 1
     assert native.moe_scatter_add(16, 256, 16, 16, 2, 2, -1, ctypes.byref(g), 16, 16, s) == 1
-    w = _native.MoeWeights(8, 16, 16, 16, 16, 16, 16)
+    w = _native.MoeWeights(8, 16, 16, 16, 16)
     assert native.moe_nvfp4_layer(16, 4, 200, 128, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
     assert native.moe_nvfp4_layer(16, 4, 256, 96, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
     assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, None, 256, 1 << 20, 16, s) == 1
@@ -73,6 +77,9 @@ def test_host_side_validation(native):
 
 
 def test_sizes(native):
+    # tiled weights: one 18 KB block per 128 rows and 256 K values, K padded up
+    assert native.nvfp4_tiled_bytes(288 * 4096, 4096) == 288 * 4096 * 4096 * 9 // 16
+    assert native.nvfp4_tiled_bytes(256, 128) == 2 * 18432
     assert native.moe_groups_bytes(1, 8, 288) > 0
     # sf region bound: (min(E, R) + ceil(R / 128)) * 128 * K / 16
     assert native.nvfp4_sf_bytes(8, 288, 4096) == (8 + 1) * 128 * 256

@@ -119,6 +119,40 @@ def test_swizzle_matches_oracle(cuda):
         assert np.array_equal(out.cpu().numpy(), O.swizzle_scales(lin))
 
 
+def expected_tiled(packed: np.ndarray, sf_linear: np.ndarray, K: int) -> np.ndarray:
+    """The GEMM tiling built independently on the host: per 128-row tile and
+    256-value stage, rows' 16-byte chunks at chunk c ^ (r % 8), then the
+    stage's scale atoms (the oracle's atom layout)."""
+    rows = packed.shape[0]
+    nk, kc4, rowb = (K + 255) // 256, K // 64, K // 2
+    pad = np.zeros((rows, nk * 128), np.uint8)
+    pad[:, :rowb] = packed
+    sw = O.swizzle_scales(sf_linear)
+    out = np.zeros(((rows // 128) * nk, 18432), np.uint8)
+    r = np.arange(128)
+    for t in range(rows // 128):
+        for ks in range(nk):
+            blk = out[t * nk + ks]
+            tile = pad[t * 128:(t + 1) * 128, ks * 128:(ks + 1) * 128].reshape(128, 8, 16)
+            img = np.zeros((128, 8, 16), np.uint8)
+            for c in range(8):
+                img[r, c ^ (r % 8)] = tile[:, c]
+            blk[:16384] = img.reshape(-1)
+            na = min(4, kc4 - 4 * ks)
+            a0 = t * kc4 + 4 * ks
+            blk[16384:16384 + na * 512] = sw[a0 * 512:(a0 + na) * 512]
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("rows,K", [(256, 256), (128, 384), (384, 128)])
+def test_tile_weights_layout(cuda, rows, K):
+    rng = np.random.default_rng(rows + K)
+    packed = rng.integers(0, 256, (1, rows, K // 2), dtype=np.uint8)
+    sfl = rng.integers(0, 256, (1, rows, K // 16), dtype=np.uint8)
+    tw = N.TiledWeight(torch.from_numpy(packed).to(cuda), torch.from_numpy(sfl).to(cuda))
+    assert np.array_equal(tw.data.cpu().numpy(), expected_tiled(packed[0], sfl[0], K))
+
+
 # ---------------------------------------------------------------------------
 # codec edge cases, and the pages' group_m = {1, 130} quantizer case
 # ---------------------------------------------------------------------------
@@ -212,7 +246,8 @@ def test_gemm_row_invariance_and_fused_w13(small):
     equals separate gate-only and up-only GEMMs; five calls bit-identical.
     Here also across MMA widths: the 140-row group runs a 128-wide and a
     16-wide MMA, the row alone a 16-wide one."""
-    E, x, ids, tw, W, *_ = small
+    E, x, ids, tw, W, w_np, _ = small
+    small_w = {k: torch.from_numpy(v).to(x.device) for k, v in w_np.items()}
     st = run_stages(x, ids, tw, W, E)
     dev = x.device
     I = W.I
@@ -226,24 +261,24 @@ def test_gemm_row_invariance_and_fused_w13(small):
         s = torch.zeros(N.sf_bytes(1, E, W.H), dtype=torch.uint8, device=dev)
         N.nvfp4_quantize_rows(xa, G1, q, s)
         d = torch.zeros(1, 2 * I, dtype=torch.float32, device=dev)
-        N.nvfp4_grouped_gemm(q, s, G1, W.w13_packed, W.w13_sf, d)
+        N.nvfp4_grouped_gemm(q, s, G1, W.w13, d)
         assert torch.equal(d[0], st["d13"][r]), r
-    # fused w13 == gate-only and up-only (gate's scale region then up's)
+    # fused w13 == gate-only and up-only GEMMs (each half tiled on its own)
     G = N.Groups(x.shape[0], ids.shape[1], E, dev)
     N.moe_route_groups(ids, E, G)
     R_max = ids.numel()
-    half = W.w13_sf.shape[1] // 2
+    w = small_w
+    gate_w = N.TiledWeight(w["w13_packed"][:, :I].contiguous(), w["w13_sf_linear"][:, :I].contiguous())
+    up_w = N.TiledWeight(w["w13_packed"][:, I:].contiguous(), w["w13_sf_linear"][:, I:].contiguous())
     gate = torch.zeros(R_max, I, dtype=torch.float32, device=dev)
     up = torch.zeros(R_max, I, dtype=torch.float32, device=dev)
-    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed[:, :I].contiguous(),
-                         W.w13_sf[:, :half].contiguous(), gate)
-    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed[:, I:].contiguous(),
-                         W.w13_sf[:, half:].contiguous(), up)
+    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, gate_w, gate)
+    N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, up_w, up)
     R = hostg["R"]
     assert torch.equal(torch.cat([gate, up], 1)[:R], st["d13"][:R])
     for _ in range(5):
         d = torch.zeros_like(st["d13"])
-        N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13_packed, W.w13_sf, d)
+        N.nvfp4_grouped_gemm(st["xq"], st["xsf"], G, W.w13, d)
         assert torch.equal(d[:R], st["d13"][:R])
 
 
