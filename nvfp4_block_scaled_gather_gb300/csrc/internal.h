@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime_api.h>
 
-#include "../../include/moe_nvfp4.h"
+#include "moe_nvfp4.h"
 
 namespace moe {
 
