@@ -67,10 +67,12 @@ enum {
 
 /* Group metadata produced by moe_route_groups (device int32 arrays, caller
  * owned; moe_groups_carve lays them out in one buffer).
- *   counts[4]            G (groups), R (rows), max Mg, total 128-row scale blocks
+ *   counts[5]            G (groups), R (rows), max Mg, total 128-row scale
+ *                        blocks, total 32-row GEMM chunks
  *   group_offsets[E+1]   first row of group g; entry G holds R
  *   group_expert[E]      expert id of group g (ascending)
  *   group_sf_block[E+1]  first 128-row scale block of group g; entry G = total
+ *   group_chunk[E+1]     first 32-row GEMM chunk of group g; entry G = total
  *   row_slot[T*k]        slot t*k+j of grouped row r (r < R)
  *   slot_row[T*k]        grouped row of slot s, or -1 for an unused slot     */
 typedef struct {
@@ -78,6 +80,7 @@ typedef struct {
   int32_t* group_offsets;
   int32_t* group_expert;
   int32_t* group_sf_block;
+  int32_t* group_chunk;
   int32_t* row_slot;
   int32_t* slot_row;
 } moe_groups_t;

@@ -20,7 +20,7 @@ c_int, c_size_t, c_void_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 
 class MoeGroups(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("counts", "group_offsets", "group_expert", "group_sf_block",
-                                       "row_slot", "slot_row")]
+                                       "group_chunk", "row_slot", "slot_row")]
 
 
 class MoeWeights(ctypes.Structure):
@@ -119,13 +119,14 @@ class Groups:
 
     def host(self) -> dict:
         """Copies the metadata to the host (synchronizes)."""
-        counts = self.view("counts", 4).cpu()
-        G, R, maxmg, nblk = (int(v) for v in counts)
+        counts = self.view("counts", 5).cpu()
+        G, R, maxmg, nblk, nchunk = (int(v) for v in counts)
         S = self.T * self.k
-        return dict(G=G, R=R, max_mg=maxmg, blocks=nblk,
+        return dict(G=G, R=R, max_mg=maxmg, blocks=nblk, chunks=nchunk,
                     group_offsets=self.view("group_offsets", G + 1).cpu(),
                     group_expert=self.view("group_expert", G).cpu(),
                     group_sf_block=self.view("group_sf_block", G + 1).cpu(),
+                    group_chunk=self.view("group_chunk", G + 1).cpu(),
                     row_slot=self.view("row_slot", R).cpu(),
                     slot_row=self.view("slot_row", S).cpu())
 

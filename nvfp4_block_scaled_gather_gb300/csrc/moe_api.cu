@@ -43,7 +43,8 @@ int* status_ptr() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool groups_ok(const moe_groups_t* g) {
-  return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->row_slot && g->slot_row;
+  return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->group_chunk &&
+         g->row_slot && g->slot_row;
 }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -124,7 +125,7 @@ size_t moe_groups_bytes(int T, int k, int E) {
   if (T < 0 || k < 0 || E < 0) return 0;
   const size_t S = (size_t)T * k;
   return align256(16 * 4) + align256(4 * (size_t)(E + 1)) + align256(4 * (size_t)E) +
-         align256(4 * (size_t)(E + 1)) + 2 * align256(4 * S);
+         2 * align256(4 * (size_t)(E + 1)) + 2 * align256(4 * S);
 }
 
 int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
@@ -136,6 +137,7 @@ int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
   g->group_offsets = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
   g->group_expert = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)E);
   g->group_sf_block = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
+  g->group_chunk = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
   g->row_slot = reinterpret_cast<int32_t*>(p); p += align256(4 * S);
   g->slot_row = reinterpret_cast<int32_t*>(p);
   return MOE_OK;

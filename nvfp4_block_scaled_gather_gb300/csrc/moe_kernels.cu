@@ -44,9 +44,9 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
   extern __shared__ int32_t smem[];
   int32_t* wc = smem;                // [32][E]: counts, then running row cursors
   int32_t* rowbase = smem + 32 * E;  // [E]: first row of each expert
-  __shared__ int32_t wsum[32][3];
+  __shared__ int32_t wsum[32][4];
   __shared__ int32_t wmax[32];
-  __shared__ int32_t tot[4];
+  __shared__ int32_t tot[5];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
 
   for (int i = tid; i < 32 * E; i += blockDim.x) wc[i] = 0;
@@ -68,42 +68,45 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
       cnt += c;
     }
   }
-  // block-wide exclusive scans of rows, group flags, 128-row scale blocks; max Mg
-  const int own0 = cnt, own1 = cnt > 0, own2 = (cnt + 127) >> 7;
-  int v0 = own0, v1 = own1, v2 = own2, mx = cnt;
+  // block-wide exclusive scans of rows, group flags, 128-row scale blocks and
+  // 32-row GEMM chunks; max Mg
+  const int own0 = cnt, own1 = cnt > 0, own2 = (cnt + 127) >> 7, own3 = (cnt + 31) >> 5;
+  int v0 = own0, v1 = own1, v2 = own2, v3 = own3, mx = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int a0 = __shfl_up_sync(~0u, v0, o), a1 = __shfl_up_sync(~0u, v1, o),
-              a2 = __shfl_up_sync(~0u, v2, o);
-    if (lane >= o) { v0 += a0; v1 += a1; v2 += a2; }
+              a2 = __shfl_up_sync(~0u, v2, o), a3 = __shfl_up_sync(~0u, v3, o);
+    if (lane >= o) { v0 += a0; v1 += a1; v2 += a2; v3 += a3; }
     mx = max(mx, __shfl_xor_sync(~0u, mx, o));
   }
-  if (lane == 31) { wsum[w][0] = v0; wsum[w][1] = v1; wsum[w][2] = v2; }
+  if (lane == 31) { wsum[w][0] = v0; wsum[w][1] = v1; wsum[w][2] = v2; wsum[w][3] = v3; }
   if (lane == 0) wmax[w] = mx;
   __syncthreads();
   if (w == 0) {
-    const int t0 = wsum[lane][0], t1 = wsum[lane][1], t2 = wsum[lane][2];
-    int i0 = t0, i1 = t1, i2 = t2, m = wmax[lane];
+    const int t0 = wsum[lane][0], t1 = wsum[lane][1], t2 = wsum[lane][2], t3 = wsum[lane][3];
+    int i0 = t0, i1 = t1, i2 = t2, i3 = t3, m = wmax[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a0 = __shfl_up_sync(~0u, i0, o), a1 = __shfl_up_sync(~0u, i1, o),
-                a2 = __shfl_up_sync(~0u, i2, o);
-      if (lane >= o) { i0 += a0; i1 += a1; i2 += a2; }
+                a2 = __shfl_up_sync(~0u, i2, o), a3 = __shfl_up_sync(~0u, i3, o);
+      if (lane >= o) { i0 += a0; i1 += a1; i2 += a2; i3 += a3; }
       m = max(m, __shfl_xor_sync(~0u, m, o));
     }
-    wsum[lane][0] = i0 - t0; wsum[lane][1] = i1 - t1; wsum[lane][2] = i2 - t2;
-    if (lane == 31) { tot[0] = i0; tot[1] = i1; tot[2] = i2; tot[3] = m; }
+    wsum[lane][0] = i0 - t0; wsum[lane][1] = i1 - t1; wsum[lane][2] = i2 - t2; wsum[lane][3] = i3 - t3;
+    if (lane == 31) { tot[0] = i0; tot[1] = i1; tot[2] = i2; tot[3] = m; tot[4] = i3; }
   }
   __syncthreads();
   if (tid < E) {
     const int row0 = v0 - own0 + wsum[w][0];
     const int gi = v1 - own1 + wsum[w][1];
     const int blk0 = v2 - own2 + wsum[w][2];
+    const int chk0 = v3 - own3 + wsum[w][3];
     rowbase[tid] = row0;
     if (cnt > 0) {
       g.group_expert[gi] = tid;
       g.group_offsets[gi] = row0;
       g.group_sf_block[gi] = blk0;
+      g.group_chunk[gi] = chk0;
     }
   }
   if (tid == 0) {
@@ -111,8 +114,10 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
     g.counts[1] = tot[0];
     g.counts[2] = tot[3];
     g.counts[3] = tot[2];
+    g.counts[4] = tot[4];
     g.group_offsets[tot[1]] = tot[0];
     g.group_sf_block[tot[1]] = tot[2];
+    g.group_chunk[tot[1]] = tot[4];
   }
   __syncthreads();
 

@@ -12,9 +12,12 @@
 //    decode group of one row costs a 16-wide MMA, not a 128-row tile. The
 //    second page ("Tiles below M=8") notes that the wasted token extent costs
 //    no HBM traffic; here it costs no tensor-core time either.
-//  * Persistent CTAs (one per SM) walk the ragged work list of
-//    (128-row activation block, 128-row weight tile) units in a fixed order;
-//    every unit streams its weight tile over the full K once.
+//  * Persistent CTAs, two per SM, walk the ragged work list of
+//    (32-token chunk of a group, 128-row weight tile) units in a fixed order;
+//    every unit streams its weight tile over the full K once. Two CTAs per SM
+//    because a CTA's tcgen05 ops (scale copies, MMAs) execute one after
+//    another: with one issuing CTA per SM the tensor pipe, not HBM, set the
+//    pace; two issuers overlap and the weight stream becomes HBM-bound.
 //  * Weights arrive pre-tiled (nvfp4_tile_weights, a load-time step): for
 //    every 128-row tile and 256-value K stage, 16 KB of e2m1 bytes already in
 //    the 128-byte-swizzled shared-memory image followed by the 2 KB of e4m3
@@ -49,10 +52,12 @@ constexpr int kATileBytes = kBM * kStageKBytes;  // 16 KB
 constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
 constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
 constexpr int kBBoxRows = 16;
+constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
-constexpr int kSmemBytes = 232448;  // 227 KB, the sm_100-family opt-in maximum
-constexpr int kTmemCols = 512;
+constexpr int kCtasPerSm = 2;
+constexpr int kSmemBytes = 114688;  // per CTA: two CTAs fit the SM's 228 KB (1 KB reserved each)
+constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
 
 struct GemmArgs {
   const uint8_t* a_sf;
@@ -62,6 +67,7 @@ struct GemmArgs {
   const int32_t* group_offsets;
   const int32_t* group_expert;
   const int32_t* group_sf_block;
+  const int32_t* group_chunk;
   int* status;
   int N, K;
   long long wait_budget;  // clock64 cycles a single wait may take
@@ -190,10 +196,12 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
   return lo;
 }
 
-// One unit of work: 128-row activation block `chunk` (a group's rows
-// [128q, 128q + 128)) against 128-row weight tile `nt` of the group's expert.
+// One unit of work: 32-row chunk `chunk` of a group (its rows [32q, 32q+32))
+// against 128-row weight tile `nt` of the group's expert. The chunk's token
+// scales sit in quarter q % 4 of a 128-row scale atom, i.e. TMEM column
+// offset q % 4 after the atom is copied with tcgen05.cp.32x128b.warpx4.
 struct Unit {
-  int row0, nvalid, nmma, nt;
+  int row0, nvalid, nmma, nt, sfb_col;
   size_t w_off, sfb_off;
 };
 
@@ -201,20 +209,21 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tile
   const int chunk = u / n_tiles;
   Unit un;
   un.nt = u - chunk * n_tiles;
-  const int gi = find_group(p.group_sf_block, G, chunk);
-  const int q = chunk - __ldg(p.group_sf_block + gi);
+  const int gi = find_group(p.group_chunk, G, chunk);
+  const int q = chunk - __ldg(p.group_chunk + gi);
   const int r0 = __ldg(p.group_offsets + gi);
   const int mg = __ldg(p.group_offsets + gi + 1) - r0;
   const int e = __ldg(p.group_expert + gi);
-  un.row0 = r0 + kBM * q;
-  un.nvalid = min(kBM, mg - kBM * q);
+  un.row0 = r0 + kTokChunk * q;
+  un.nvalid = min(kTokChunk, mg - kTokChunk * q);
   un.nmma = (un.nvalid + 15) & ~15;
+  un.sfb_col = q & 3;
   un.w_off = ((size_t)e * n_tiles + un.nt) * nk * kWStageBytes;
-  un.sfb_off = (size_t)chunk * kc4 * kAtomBytes;
+  un.sfb_off = (size_t)(__ldg(p.group_sf_block + gi) + (q >> 2)) * kc4 * kAtomBytes;
   return un;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -234,12 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- schedule shape, identical on every thread ----
   const int G = __ldg(p.counts + 0);
   const int maxmg = __ldg(p.counts + 2);
-  const int nblk = G > 0 ? __ldg(p.group_sf_block + G) : 0;
+  const int nchunks = G > 0 ? __ldg(p.group_chunk + G) : 0;
   const int n_tiles = p.N / kBM;
-  const int total_units = nblk * n_tiles;
+  const int total_units = nchunks * n_tiles;
   const int kc4 = p.K / 64;               // scale atoms along K per 128-row block
   const int nk = (p.K + 255) / 256;       // stages per unit
-  const int tn = min(kBM, max(16, (maxmg + 15) & ~15));   // token rows per B stage
+  const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
   const int acc_cols = max(32, tn);
   const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
   const int avail = kSmemBytes - 1024 - 1024;
@@ -340,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < natoms; ++a) {
             const uint64_t adesc = desc_sw128(sWs + 32 * a);
             const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a + un.sfb_col,
+                        (ks | a) != 0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -434,14 +444,20 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
   p.group_offsets = g.group_offsets;
   p.group_expert = g.group_expert;
   p.group_sf_block = g.group_sf_block;
+  p.group_chunk = g.group_chunk;
   p.status = status;
   p.N = N;
   p.K = K;
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  const long long units_bound = sf_blocks_bound(R_max, E < R_max ? E : R_max) * (N / kBM);
-  const int grid = (int)(units_bound < num_sms() ? units_bound : num_sms());
+  const long long chunks_bound = (long long)(E < R_max ? E : R_max) + (R_max + kTokChunk - 1) / kTokChunk;
+  const long long units_bound = chunks_bound * (N / kBM);
+  const long long slots = (long long)num_sms() * kCtasPerSm;
+  const int grid = (int)(units_bound < slots ? units_bound : slots);
   gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmB, p);
   return cudaGetLastError();
 }

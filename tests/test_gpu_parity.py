@@ -37,6 +37,8 @@ def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
     assert np.array_equal(host["group_offsets"].numpy(), ref_offs)
     assert np.array_equal(host["row_slot"].numpy(), ref_row_slot)
     assert np.array_equal(host["group_sf_block"].numpy(), O.group_sf_blocks(ref_offs))
+    chunks = np.concatenate([[0], np.cumsum((np.diff(ref_offs) + 31) // 32)])
+    assert np.array_equal(host["group_chunk"].numpy(), chunks) and host["chunks"] == chunks[-1]
     assert host["max_mg"] == (int(np.diff(ref_offs).max()) if G else 0)
     slot_row = np.full(S, -1)
     slot_row[ref_row_slot] = np.arange(len(ref_row_slot))
