@@ -218,10 +218,10 @@ def gpu_bench(args, rank, world):
         S = T_max * c.k
         G_ = N.Groups(T_max, c.k, c.E, dev)
         xq = torch.empty(S, c.H // 2, dtype=torch.uint8, device=dev)
-        xsf = torch.empty(N.sf_bytes(S, c.E, c.H), dtype=torch.uint8, device=dev)
+        xsf = torch.empty(N.sf_bytes(S, c.E, c.H, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
         d13 = torch.empty(S, 2 * c.I, dtype=torch.float32, device=dev)
         hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
-        hsf = torch.empty(N.sf_bytes(S, c.E, c.I), dtype=torch.uint8, device=dev)
+        hsf = torch.empty(N.sf_bytes(S, c.E, c.I, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
         d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
         names = ["route", "gather_quantize", "gemm_w13", "swiglu_quantize", "gemm_w2", "scatter"]
         acc = {n: [] for n in names}

@@ -65,6 +65,19 @@ enum {
   MOE_ERR_WORKSPACE = 5  /* workspace smaller than moe_nvfp4_layer_workspace_size() */
 };
 
+/* Token-scale layouts (the e4m3 scales of quantized activation rows).
+ *   MOE_SF_ATOM128: per group, 128-row atoms as above, each group's region
+ *     zero-padded to a multiple of 128 rows (the CUTLASS SFA layout the first
+ *     page's kernels wrote; nvfp4_sf_bytes() bytes).
+ *   MOE_SF_CHUNK32: what nvfp4_grouped_gemm reads. Rows of each group are cut
+ *     into 32-row chunks (chunk c = counts-order index from group_chunk); for
+ *     chunk c and K-atom a (64 values) a 512-byte block at (c*(K/64) + a)*512
+ *     whose 16-byte row i holds, in its first 4 bytes, the scales of chunk row
+ *     i for K-blocks 4a..4a+3; all other bytes are zero. Each block is what one
+ *     tcgen05.cp.32x128b.warpx4 copies for a token operand of up to 32 rows.
+ * Both regions are 128*(K/16) bytes per block (128-row atom or 32-row chunk). */
+enum { MOE_SF_ATOM128 = 0, MOE_SF_CHUNK32 = 1 };
+
 /* Group metadata produced by moe_route_groups (device int32 arrays, caller
  * owned; moe_groups_carve lays them out in one buffer).
  *   counts[5]            G (groups), R (rows), max Mg, total 128-row scale
@@ -113,10 +126,11 @@ int moe_nvfp4_check_status(cudaStream_t stream);
 size_t moe_groups_bytes(int T, int k, int E);
 int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* groups /* host */);
 
-/* Bytes of a per-group padded scale region able to hold any grouping of up to
- * R_max rows over E experts for a K-wide operand:
- * (min(E, R_max) + ceil(R_max/128)) * 128 * K/16. */
-size_t nvfp4_sf_bytes(int R_max, int E, int K);
+/* Bytes of a token-scale region (layout MOE_SF_ATOM128 or MOE_SF_CHUNK32)
+ * able to hold any grouping of up to R_max rows over E experts for a K-wide
+ * operand: (min(E, R_max) + ceil(R_max/128)) * 128 * K/16 for ATOM128,
+ * (min(E, R_max) + ceil(R_max/32)) * 128 * K/16 for CHUNK32. */
+size_t nvfp4_sf_bytes(int R_max, int E, int K, int layout);
 
 /* a1 -- route-group. Counts the T*k slots per expert, scans, and places rows
  * stably by (expert ascending, slot ascending); fills *groups on the device.
@@ -134,23 +148,26 @@ int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, in
                     const moe_groups_t* groups, uint16_t* xg, cudaStream_t stream);
 
 /* a3 / a6 -- nvfp4_quantize_rows: grouped bf16 rows [R_max, K] -> packed
- * [R_max, K/2] (rows >= R untouched) and the per-group padded scale region
- * `sf` (nvfp4_sf_bytes(R_max, E, K) bytes; padding bytes written as 0).
- * E is the expert count the groups were built for. First page, "What
+ * [R_max, K/2] (rows >= R untouched) and the token scales `sf` in `layout`
+ * (nvfp4_sf_bytes(R_max, E, K, layout) bytes; bytes no row fills are written
+ * as 0). E is the expert count the groups were built for. First page, "What
  * changed" and "Proof" (byte-for-byte vs the host codec, group_m = {1, 130}).
  * K % 64 == 0. */
-int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups,
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups, int layout,
                         uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
 /* a2 + a3 fused: quantizes x[row_slot[r]/k, :] straight into grouped NVFP4
  * rows; output identical to moe_gather_rows followed by nvfp4_quantize_rows. */
 int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups,
-                             uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+                             int layout, uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
 /* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
  * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
  * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
- * W [E, N, K] comes tiled by nvfp4_tile_weights. One launch for all groups on
+ * a_sf is in MOE_SF_CHUNK32. W [E, N, K] comes tiled by nvfp4_tile_weights.
+ * A group larger than 32 rows is processed as ceil(Mg/32) chunks, each
+ * streaming the expert's weights (decode groups hold at most a few dozen
+ * rows). One launch for all groups on
  * tcgen05 block-scaled MMA (kind::mxf4nvf4, scale vector 16), accumulators in
  * tensor memory. First page, "What changed": grouped GEMM w13 N=4096 K=4096
  * and w2 N=4096 K=2048, alpha = 1. N % 128 == 0, K % 64 == 0; every pointer
@@ -167,12 +184,11 @@ int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t
                    const float* g_gate_up, uint16_t* h, cudaStream_t stream);
 
 /* a5 + a6 fused: SwiGLU as swiglu_grouped, then the a3 codec on the bf16 h,
- * written as packed [R_max, I/2] + per-group padded scales
- * (nvfp4_sf_bytes(R_max, E, I) bytes). Identical to swiglu_grouped followed
- * by nvfp4_quantize_rows. */
-int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups,
-                            const float* g_gate_up, uint8_t* packed, uint8_t* sf,
-                            cudaStream_t stream);
+ * written as packed [R_max, I/2] + token scales in `layout`
+ * (nvfp4_sf_bytes(R_max, E, I, layout) bytes). Identical to swiglu_grouped
+ * followed by nvfp4_quantize_rows. */
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, int layout,
+                            const float* g_gate_up, uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
 /* a8 -- moe_scatter_add: y[t, :] = sum over t's used slots, in ascending
  * grouped-row order (= ascending expert id), of topk_w[t, j] * g_down[e] *

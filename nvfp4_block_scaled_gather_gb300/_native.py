@@ -17,6 +17,10 @@ _LIB = None
 
 c_int, c_size_t, c_void_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 
+# token-scale layouts (include/moe_nvfp4.h)
+SF_ATOM128 = 0   # per group, 128-row atoms, zero-padded (the pages' CUTLASS layout)
+SF_CHUNK32 = 1   # per 32-row chunk, the layout nvfp4_grouped_gemm reads
+
 
 class MoeGroups(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("counts", "group_offsets", "group_expert", "group_sf_block",
@@ -33,20 +37,20 @@ _SIGS = {
     "moe_nvfp4_check_status": (c_int, [c_void_p]),
     "moe_groups_bytes": (c_size_t, [c_int, c_int, c_int]),
     "moe_groups_carve": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups)]),
-    "nvfp4_sf_bytes": (c_size_t, [c_int, c_int, c_int]),
+    "nvfp4_sf_bytes": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_route_groups": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p]),
     "moe_gather_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, ctypes.POINTER(MoeGroups),
                                 c_void_p, c_void_p]),
-    "nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
+    "nvfp4_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int, c_void_p,
                                     c_void_p, c_void_p]),
-    "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(MoeGroups),
+    "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
                                          c_void_p, c_void_p, c_void_p]),
     "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int, c_int,
                                    c_int, c_void_p, c_void_p]),
     "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
                                c_void_p]),
-    "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p,
-                                        c_void_p, c_void_p, c_void_p]),
+    "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
+                                        c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                 ctypes.POINTER(MoeGroups), c_void_p, c_void_p, c_void_p]),
     "moe_nvfp4_layer_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
@@ -131,8 +135,8 @@ class Groups:
                     slot_row=self.view("slot_row", S).cpu())
 
 
-def sf_bytes(R_max: int, E: int, K: int) -> int:
-    return load().nvfp4_sf_bytes(R_max, E, K)
+def sf_bytes(R_max: int, E: int, K: int, layout: int = SF_CHUNK32) -> int:
+    return load().nvfp4_sf_bytes(R_max, E, K, layout)
 
 
 def check_status(stream=None) -> int:
@@ -152,18 +156,18 @@ def moe_gather_rows(x, topk_ids, E: int, groups: Groups, xg, stream=None):
                                                      ctypes.byref(groups.struct), _ptr(xg), _stream(stream)))
 
 
-def nvfp4_quantize_rows(rows, groups: Groups, packed, sf, stream=None):
+def nvfp4_quantize_rows(rows, groups: Groups, packed, sf, layout: int = SF_CHUNK32, stream=None):
     R, K = rows.shape
     _check("nvfp4_quantize_rows", load().nvfp4_quantize_rows(_ptr(rows), R, K, groups.E,
-                                                             ctypes.byref(groups.struct), _ptr(packed), _ptr(sf),
-                                                             _stream(stream)))
+                                                             ctypes.byref(groups.struct), layout, _ptr(packed),
+                                                             _ptr(sf), _stream(stream)))
 
 
-def moe_gather_quantize_rows(x, k: int, groups: Groups, packed, sf, stream=None):
+def moe_gather_quantize_rows(x, k: int, groups: Groups, packed, sf, layout: int = SF_CHUNK32, stream=None):
     T, H = x.shape
     _check("moe_gather_quantize_rows",
-           load().moe_gather_quantize_rows(_ptr(x), T, H, k, groups.E, ctypes.byref(groups.struct), _ptr(packed),
-                                           _ptr(sf), _stream(stream)))
+           load().moe_gather_quantize_rows(_ptr(x), T, H, k, groups.E, ctypes.byref(groups.struct), layout,
+                                           _ptr(packed), _ptr(sf), _stream(stream)))
 
 
 class TiledWeight:
@@ -195,10 +199,10 @@ def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):
                                                    _ptr(g_gate_up), _ptr(h), _stream(stream)))
 
 
-def swiglu_quantize_grouped(d13, groups: Groups, g_gate_up, packed, sf, stream=None):
+def swiglu_quantize_grouped(d13, groups: Groups, g_gate_up, packed, sf, layout: int = SF_CHUNK32, stream=None):
     R_max, I2 = d13.shape
     _check("swiglu_quantize_grouped",
-           load().swiglu_quantize_grouped(_ptr(d13), R_max, I2 // 2, groups.E, ctypes.byref(groups.struct),
+           load().swiglu_quantize_grouped(_ptr(d13), R_max, I2 // 2, groups.E, ctypes.byref(groups.struct), layout,
                                           _ptr(g_gate_up), _ptr(packed), _ptr(sf), _stream(stream)))
 
 

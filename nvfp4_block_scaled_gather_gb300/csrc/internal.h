@@ -18,6 +18,20 @@ inline long long sf_blocks_bound(long long R_max, long long G_max) {
   long long g = G_max < R_max ? G_max : R_max;
   return g + (R_max + 127) / 128;
 }
+// Upper bound on 32-row GEMM chunks for R_max rows in at most G_max groups.
+inline long long chunks_bound(long long R_max, long long G_max) {
+  long long g = G_max < R_max ? G_max : R_max;
+  return g + (R_max + 31) / 32;
+}
+// Row blocks of a token-scale layout (128-row atoms or 32-row chunks).
+inline long long row_blocks_bound(long long R_max, long long G_max, int layout) {
+  return layout == MOE_SF_ATOM128 ? sf_blocks_bound(R_max, G_max) : chunks_bound(R_max, G_max);
+}
+// Bytes of a token-scale region for K-wide rows (both layouts: rows x K/16).
+inline size_t token_sf_bytes(long long R_max, long long G_max, long long K, int layout) {
+  return layout == MOE_SF_ATOM128 ? (size_t)sf_blocks_bound(R_max, G_max) * 128 * (K / 16)
+                                  : (size_t)chunks_bound(R_max, G_max) * 32 * (K / 64) * 16;
+}
 
 int num_sms();  // SM count of the current device (cached per device)
 
@@ -28,9 +42,9 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 // src_k > 0: rows are x[row_slot[r] / src_k]; src_k == 0: rows are src[r].
 // E bounds the group count (grid size); CTAs past the routed blocks exit.
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
-                            const moe_groups_t& g, uint8_t* packed, uint8_t* sf, cudaStream_t s);
+                            const moe_groups_t& g, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
 // h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
-cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g,
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
                           const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf,
                           cudaStream_t s);
 // Load-time weight tiling for the grouped GEMM (rows % 128 == 0).

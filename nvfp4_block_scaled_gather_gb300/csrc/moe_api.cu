@@ -49,6 +49,8 @@ bool groups_ok(const moe_groups_t* g) {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+bool layout_ok(int layout) { return layout == MOE_SF_ATOM128 || layout == MOE_SF_CHUNK32; }
+
 struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
@@ -60,7 +62,6 @@ struct LayerWs {
 LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   LayerWs w;
   const size_t S = (size_t)T * k;
-  const long long nblk = sf_blocks_bound((long long)S, E);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
@@ -70,10 +71,10 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   uint8_t* gmem = take(moe_groups_bytes(T, k, E));
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
-  w.xsf = take((size_t)nblk * 128 * (H / 16));
+  w.xsf = take(token_sf_bytes((long long)S, E, H, MOE_SF_CHUNK32));
   w.d13 = reinterpret_cast<float*>(take(S * 2 * I * sizeof(float)));
   w.hq = take(S * I / 2);
-  w.hsf = take((size_t)nblk * 128 * (I / 16));
+  w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
   w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
   w.bytes = off;
   return w;
@@ -143,9 +144,9 @@ int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
   return MOE_OK;
 }
 
-size_t nvfp4_sf_bytes(int R_max, int E, int K) {
-  if (R_max < 0 || E < 0 || K < 0) return 0;
-  return (size_t)sf_blocks_bound(R_max, E) * 128 * (K / 16);
+size_t nvfp4_sf_bytes(int R_max, int E, int K, int layout) {
+  if (R_max < 0 || E < 0 || K < 0 || (layout != MOE_SF_ATOM128 && layout != MOE_SF_CHUNK32)) return 0;
+  return token_sf_bytes(R_max, E, K, layout);
 }
 
 int moe_route_groups(const int32_t* topk_ids, int T, int k, int E, const moe_groups_t* groups, cudaStream_t stream) {
@@ -164,23 +165,25 @@ int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, in
   return status_of(launch_gather(x, H, k, T * k, *groups, xg, stream));
 }
 
-int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups,
+int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe_groups_t* groups, int layout,
                         uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || K <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID;
+  if (!groups_ok(groups) || R_max < 0 || K <= 0 || E <= 0 || E > kMaxExperts || !layout_ok(layout))
+    return MOE_ERR_INVALID;
   if (K % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!rows || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_quantize(rows, 0, R_max, E, K, *groups, packed, sf, stream));
+  return status_of(launch_quantize(rows, 0, R_max, E, K, *groups, layout, packed, sf, stream));
 }
 
-int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups,
+int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups, int layout,
                              uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || E <= 0 || E > kMaxExperts)
+  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || E <= 0 || E > kMaxExperts ||
+      !layout_ok(layout))
     return MOE_ERR_INVALID;
   if (H % 64) return MOE_ERR_SHAPE;
   if (T * k == 0) return MOE_OK;
   if (!x || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_quantize(x, k, T * k, E, H, *groups, packed, sf, stream));
+  return status_of(launch_quantize(x, k, T * k, E, H, *groups, layout, packed, sf, stream));
 }
 
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
@@ -204,16 +207,17 @@ int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, E, I, *groups, g_gate_up, h, nullptr, nullptr, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
 }
 
-int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups,
+int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, int layout,
                             const float* g_gate_up, uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || I <= 0 || E <= 0 || E > kMaxExperts) return MOE_ERR_INVALID;
+  if (!groups_ok(groups) || R_max < 0 || I <= 0 || E <= 0 || E > kMaxExperts || !layout_ok(layout))
+    return MOE_ERR_INVALID;
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, E, I, *groups, g_gate_up, nullptr, packed, sf, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
 }
 
 int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k, int E,
@@ -252,11 +256,11 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (!st) return MOE_ERR_CUDA;
   const int S = T * k;
   cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
-  if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, ws.xq, ws.xsf, stream);
+  if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
   if (err == cudaSuccess)
     err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, st, stream);
   if (err == cudaSuccess)
-    err = launch_swiglu(ws.d13, S, E, I, ws.groups, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
+    err = launch_swiglu(ws.d13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
   if (err == cudaSuccess)
     err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, st, stream);
   if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);

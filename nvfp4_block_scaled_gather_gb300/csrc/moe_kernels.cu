@@ -168,8 +168,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
 // Lanes that are not `active` compute along (shuffles need the full warp) but
 // write nothing; a 16-lane group is either wholly active or wholly not.
 __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool active, int lane,
-                                                    uint8_t* __restrict__ packed_dst, uint8_t* __restrict__ sf_blk,
-                                                    int m, int c, int Kc) {
+                                                    uint8_t* __restrict__ packed_dst, uint32_t* __restrict__ word) {
   float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
@@ -184,61 +183,82 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
                  s3 = __shfl_down_sync(~0u, s, 12);
   if (!active) return;
   *reinterpret_cast<uint16_t*>(packed_dst) = (uint16_t)codes;
-  if ((lane & 15) == 0)
-    *reinterpret_cast<uint32_t*>(sf_blk + sf_atom_offset(m, c, Kc)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  if ((lane & 15) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
-// The CTA's 128-row scale block `blk`: first grouped row, valid rows and group.
+// Token-scale layouts (include/moe_nvfp4.h): per group 128-row atoms, or per
+// 32-row GEMM chunk one 512-byte atom per 64 K values whose 16-byte row i
+// holds chunk row i's four scales in its first word (other words zero).
+constexpr int kRowsAtom = 128, kRowsChunk = 32;
+
+struct ScaleTarget {
+  uint8_t* base;  // the CTA's row block region
+  int layout, Kc;
+  // word holding scale columns c..c+3 (c % 4 == 0) of row m of the block
+  __device__ __forceinline__ uint32_t* word(int m, int c) const {
+    const uint32_t off = layout == MOE_SF_ATOM128 ? sf_atom_offset(m, c, Kc) : (uint32_t)(c >> 2) * 512u + m * 16u;
+    return reinterpret_cast<uint32_t*>(base + off);
+  }
+  // zero every word of atoms [a0, a0 + na) that no real row (< nvalid) fills
+  __device__ __forceinline__ void zero_rest(int a0, int na, int nvalid) const {
+    uint32_t* words = reinterpret_cast<uint32_t*>(base + (size_t)a0 * 512);
+    for (int w = threadIdx.x; w < na * 128; w += blockDim.x) {
+      const int wi = w & 127;
+      const bool real = layout == MOE_SF_ATOM128 ? (wi >> 2) + 32 * (wi & 3) < nvalid  // row (wi/4) + 32*(wi%4)
+                                                 : ((wi & 3) == 0 && (wi >> 2) < nvalid);
+      if (!real) words[w] = 0u;
+    }
+  }
+};
+
+// The CTA's row block `blk` (128 rows per block in the atom layout, 32 in the
+// chunk layout): first grouped row, valid rows and group.
 struct RowBlock {
   int row0, nvalid, gi;
 };
 
-__device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int blk) {
+__device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int layout, int blk) {
   __shared__ int s_info[3];
   if (threadIdx.x == 0) {
     const int G = __ldg(g.counts + 0);
-    const int gi = find_group(g.group_sf_block, G, blk);
-    const int m0 = (blk - __ldg(g.group_sf_block + gi)) * 128;
+    const int32_t* starts = layout == MOE_SF_ATOM128 ? g.group_sf_block : g.group_chunk;
+    const int rows = layout == MOE_SF_ATOM128 ? kRowsAtom : kRowsChunk;
+    const int gi = find_group(starts, G, blk);
+    const int m0 = (blk - __ldg(starts + gi)) * rows;
     const int r0 = __ldg(g.group_offsets + gi);
     const int mg = __ldg(g.group_offsets + gi + 1) - r0;
     s_info[0] = r0 + m0;
-    s_info[1] = min(128, mg - m0);
+    s_info[1] = min(rows, mg - m0);
     s_info[2] = gi;
   }
   __syncthreads();
   return RowBlock{s_info[0], s_info[1], s_info[2]};
 }
 
-// Zeroes the scale words of padding rows (>= nvalid) of a block's atoms
-// [a0, a0 + na); real rows' words are written by the quantizing lanes.
-__device__ __forceinline__ void zero_padding_words(uint8_t* __restrict__ sf_blk, int a0, int na, int nvalid) {
-  uint32_t* words = reinterpret_cast<uint32_t*>(sf_blk + (size_t)a0 * 512);
-  for (int w = threadIdx.x; w < na * 128; w += blockDim.x) {
-    const int wi = w & 127;                    // word wi of an atom holds row (wi/4) + 32*(wi%4)
-    if ((wi >> 2) + 32 * (wi & 3) >= nvalid) words[w] = 0u;
-  }
+__device__ __forceinline__ int routed_blocks(const moe_groups_t& g, int layout) {
+  return __ldg(g.counts + (layout == MOE_SF_ATOM128 ? 3 : 4));
 }
 
 constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K)
 
 // ---------------------------------------------------------------------------
-// a3 / a6 quantize (with optional a2 gather). Grid: (128-row scale block,
-// 1024-value column chunk); CTAs past the routed block count exit. Each lane
-// quantizes 4 values; padding rows of the block get zero scale words.
+// a3 / a6 quantize (with optional a2 gather). Grid: (row block, 1024-value
+// column chunk); CTAs past the routed block count exit. Each lane quantizes 4
+// values; scale words no real row fills are zeroed.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k, int K,
-                                                            moe_groups_t g, uint8_t* __restrict__ packed,
+                                                            moe_groups_t g, int layout, uint8_t* __restrict__ packed,
                                                             uint8_t* __restrict__ sf) {
   const int blk = blockIdx.x;
-  if (blk >= __ldg(g.counts + 3)) return;
-  const RowBlock rb = resolve_block(g, blk);
+  if (blk >= routed_blocks(g, layout)) return;
+  const RowBlock rb = resolve_block(g, layout, blk);
   const int Kc = K / 16;
   const int kc0 = blockIdx.y * kColsPerCta;
   const int kcount = min(kColsPerCta, K - kc0);
   const int quads = kcount / 4;
   const int total = rb.nvalid * quads;
   const int lane = threadIdx.x & 31;
-  uint8_t* sf_blk = sf + (size_t)blk * 128 * Kc;
+  const ScaleTarget st{sf + (size_t)blk * 128 * Kc, layout, Kc};  // either layout: 128*Kc bytes per block
   for (int base = (threadIdx.x & ~31); base < total; base += blockDim.x) {
     const int item = base + lane;
     const bool active = item < total;
@@ -254,10 +274,10 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
       v[2] = bf16_to_f32(u.y & 0xFFFFu);
       v[3] = bf16_to_f32(u.y >> 16);
     }
-    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2, sf_blk, m,
-                        (kc0 + 4 * q) / 16, Kc);
+    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2,
+                        st.word(m, (kc0 + 4 * q) / 16));
   }
-  zero_padding_words(sf_blk, kc0 / 64, kcount / 64, rb.nvalid);
+  st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
 }
 
 // ---------------------------------------------------------------------------
@@ -265,12 +285,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
 // over the I-wide output. Each lane reads 4 gate and 4 up fp32 values.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int I, moe_groups_t g,
-                                                          const float* __restrict__ g_gate_up,
+                                                          int layout, const float* __restrict__ g_gate_up,
                                                           uint16_t* __restrict__ h, uint8_t* __restrict__ packed,
                                                           uint8_t* __restrict__ sf) {
   const int blk = blockIdx.x;
-  if (blk >= __ldg(g.counts + 3)) return;
-  const RowBlock rb = resolve_block(g, blk);
+  if (blk >= routed_blocks(g, layout)) return;
+  const RowBlock rb = resolve_block(g, layout, blk);
   const int e = __ldg(g.group_expert + rb.gi);
   const float gg = __ldg(g_gate_up + 2 * e), gu = __ldg(g_gate_up + 2 * e + 1);
   const int Kc = I / 16;
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
   const int quads = kcount / 4;
   const int total = rb.nvalid * quads;
   const int lane = threadIdx.x & 31;
-  uint8_t* sf_blk = h ? nullptr : sf + (size_t)blk * 128 * Kc;
+  const ScaleTarget st{h ? nullptr : sf + (size_t)blk * 128 * Kc, layout, Kc};
   for (int base = (threadIdx.x & ~31); base < total; base += blockDim.x) {
     const int item = base + lane;
     const bool active = item < total;
@@ -306,11 +326,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
         *reinterpret_cast<uint2*>(h + (size_t)r * I + kc0 + 4 * q) = make_uint2(lo, hi);
       }
     } else {
-      quantize_quad_store(v, active, lane, packed + (size_t)r * (I / 2) + (kc0 + 4 * q) / 2, sf_blk, m,
-                          (kc0 + 4 * q) / 16, Kc);
+      quantize_quad_store(v, active, lane, packed + (size_t)r * (I / 2) + (kc0 + 4 * q) / 2,
+                          st.word(m, (kc0 + 4 * q) / 16));
     }
   }
-  if (!h) zero_padding_words(sf_blk, kc0 / 64, kcount / 64, rb.nvalid);
+  if (!h) st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
 }
 
 // ---------------------------------------------------------------------------
@@ -444,16 +464,16 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 }
 
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K, const moe_groups_t& g,
-                            uint8_t* packed, uint8_t* sf, cudaStream_t s) {
-  const dim3 grid((unsigned)sf_blocks_bound(R_max, E), (K + kColsPerCta - 1) / kColsPerCta);
-  quantize_kernel<<<grid, kThreads, 0, s>>>(src, src_k, K, g, packed, sf);
+                            int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
+  const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kColsPerCta - 1) / kColsPerCta);
+  quantize_kernel<<<grid, kThreads, 0, s>>>(src, src_k, K, g, layout, packed, sf);
   return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, const float* g_gate_up,
-                          uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
-  const dim3 grid((unsigned)sf_blocks_bound(R_max, E), (I + kColsPerCta - 1) / kColsPerCta);
-  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, I, g, g_gate_up, h, packed, sf);
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
+                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
+  const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (I + kColsPerCta - 1) / kColsPerCta);
+  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, I, g, layout, g_gate_up, h, packed, sf);
   return cudaGetLastError();
 }
 

@@ -146,6 +146,16 @@ __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[1
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
@@ -198,10 +208,10 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
 
 // One unit of work: 32-row chunk `chunk` of a group (its rows [32q, 32q+32))
 // against 128-row weight tile `nt` of the group's expert. The chunk's token
-// scales sit in quarter q % 4 of a 128-row scale atom, i.e. TMEM column
-// offset q % 4 after the atom is copied with tcgen05.cp.32x128b.warpx4.
+// scales are one 512-byte block per K-atom (layout MOE_SF_CHUNK32), copied to
+// TMEM with tcgen05.cp.32x128b.warpx4 at a 4-column-aligned address.
 struct Unit {
-  int row0, nvalid, nmma, nt, sfb_col;
+  int row0, nvalid, nmma, nt;
   size_t w_off, sfb_off;
 };
 
@@ -217,9 +227,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tile
   un.row0 = r0 + kTokChunk * q;
   un.nvalid = min(kTokChunk, mg - kTokChunk * q);
   un.nmma = (un.nvalid + 15) & ~15;
-  un.sfb_col = q & 3;
   un.w_off = ((size_t)e * n_tiles + un.nt) * nk * kWStageBytes;
-  un.sfb_off = (size_t)(__ldg(p.group_sf_block + gi) + (q >> 2)) * kc4 * kAtomBytes;
+  un.sfb_off = (size_t)chunk * kc4 * kAtomBytes;
   return un;
 }
 
@@ -349,8 +358,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           for (int a = 0; a < natoms; ++a) {
             const uint64_t adesc = desc_sw128(sWs + 32 * a);
             const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a + un.sfb_col,
-                        (ks | a) != 0);
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -380,13 +388,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int n = un.nt * kBM + quad * 32 + lane;
       float* dcol = p.d + (size_t)un.row0 * p.N + n;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
-      for (int c0 = 0; c0 < un.nvalid; c0 += 16) {
+      // one load of 16 or 32 columns from the buffer's first column (aligned)
+      if (un.nvalid <= 16) {
         uint32_t r[16];
-        tc_ld_32x32b_x16(taddr + c0, r);
+        tc_ld_32x32b_x16(taddr, r);
         tc_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (c0 + j < un.nvalid) dcol[(size_t)(c0 + j) * p.N] = __uint_as_float(r[j]);
+          if (j < un.nvalid) dcol[(size_t)j * p.N] = __uint_as_float(r[j]);
+      } else {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(taddr, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < un.nvalid) dcol[(size_t)j * p.N] = __uint_as_float(r[j]);
       }
       tc_fence_before();
       mbar_arrive(acce_bar(acc));

@@ -49,6 +49,40 @@ def oracle_weights(w: dict) -> dict:
     return out
 
 
+def row_scales(sf_atom: np.ndarray, offs: np.ndarray, K: int) -> np.ndarray:
+    """Per-row scale codes [R, K/16] read out of the oracle's 128-row atom
+    region (the oracle's own layout function)."""
+    from oracle import nvfp4_moe as O
+    Kc = K // 16
+    blocks = O.group_sf_blocks(offs)
+    out = np.zeros((int(offs[-1]), Kc), np.uint8)
+    for g in range(len(offs) - 1):
+        m = np.arange(int(offs[g + 1] - offs[g]))
+        mm, cc = np.meshgrid(m, np.arange(Kc), indexing="ij")
+        out[offs[g] + m] = sf_atom[int(blocks[g]) * 128 * Kc + O.sf_atom_offset(mm, cc, Kc)]
+    return out
+
+
+def chunk32_bytes(scales: np.ndarray, offs: np.ndarray, K: int) -> np.ndarray:
+    """The MOE_SF_CHUNK32 token-scale region for these per-row scales, built
+    from its definition: 32-row chunks per group, one 512-byte block per 64 K
+    values, row i of a block = [chunk row i's 4 scales, 12 zero bytes]."""
+    na = K // 64
+    mg = np.diff(offs)
+    nch = (mg + 31) // 32
+    out = np.zeros(int(nch.sum()) * na * 512, np.uint8)
+    c = 0
+    for g in range(len(mg)):
+        for q in range(int(nch[g])):
+            rows = np.arange(offs[g] + 32 * q, min(offs[g + 1], offs[g] + 32 * q + 32))
+            for i, r in enumerate(rows):
+                for a in range(na):
+                    o = (c * na + a) * 512 + i * 16
+                    out[o:o + 4] = scales[r, 4 * a:4 * a + 4]
+            c += 1
+    return out
+
+
 def run_stages(x, ids, tw, W: N.Weights, E: int) -> dict:
     """The layer through the separate entry points (unfused)."""
     T, H = x.shape

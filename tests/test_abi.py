@@ -57,8 +57,9 @@ def test_host_side_validation(native):
     # missing group arrays / bad sizes / misaligned weights
     assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 4, 128, 256, 16, s) == 1
     assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 24, 4, 128, 256, 16, s) == 1
-    assert native.nvfp4_quantize_rows(16, 8, 100, 4, ctypes.byref(g), 16, 16, s) == 2
-    assert native.nvfp4_quantize_rows(16, 8, 128, 0, ctypes.byref(g), 16, 16, s) == 1
+    assert native.nvfp4_quantize_rows(16, 8, 100, 4, ctypes.byref(g), 1, 16, 16, s) == 2
+    assert native.nvfp4_quantize_rows(16, 8, 128, 0, ctypes.byref(g), 1, 16, 16, s) == 1
+    assert native.nvfp4_quantize_rows(16, 8, 128, 4, ctypes.byref(g), 7, 16, 16, s) == 1
     assert native.nvfp4_tile_weights(16, 16, 100, 128, 16, s) == 2
     assert native.nvfp4_tile_weights(16, 16, 128, 96, 16, s) == 2
     assert native.moe_route_groups(16, 2, 2, 2000, ctypes.byref(g), s) == 1
@@ -81,9 +82,11 @@ def test_sizes(native):
     assert native.nvfp4_tiled_bytes(288 * 4096, 4096) == 288 * 4096 * 4096 * 9 // 16
     assert native.nvfp4_tiled_bytes(256, 128) == 2 * 18432
     assert native.moe_groups_bytes(1, 8, 288) > 0
-    # sf region bound: (min(E, R) + ceil(R / 128)) * 128 * K / 16
-    assert native.nvfp4_sf_bytes(8, 288, 4096) == (8 + 1) * 128 * 256
-    assert native.nvfp4_sf_bytes(2304, 288, 2048) == (288 + 18) * 128 * 128
+    # token-scale region bounds: (min(E, R) + ceil(R / 128 or 32)) * 128 * K / 16
+    assert native.nvfp4_sf_bytes(8, 288, 4096, 0) == (8 + 1) * 128 * 256
+    assert native.nvfp4_sf_bytes(2304, 288, 2048, 0) == (288 + 18) * 128 * 128
+    assert native.nvfp4_sf_bytes(2304, 288, 2048, 1) == (288 + 72) * 128 * 128
+    assert native.nvfp4_sf_bytes(8, 288, 4096, 5) == 0
     small = native.moe_nvfp4_layer_workspace_size(1, 8, 288, 4096, 2048)
     big = native.moe_nvfp4_layer_workspace_size(288, 8, 288, 4096, 2048)
     assert 0 < small < big

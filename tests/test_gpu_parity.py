@@ -17,8 +17,8 @@ from nvfp4_block_scaled_gather_gb300 import _native as N
 from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_layer, make_weights, make_activations, \
     make_routing
 from oracle import nvfp4_moe as O
-from tests.gpu_cases import (LazyExperts, bf16_to_np, bf16_ulps, np_to_bf16, oracle_weights, rel_fro, run_stages,
-                             small_case, weights_from)
+from tests.gpu_cases import (LazyExperts, bf16_to_np, bf16_ulps, chunk32_bytes, np_to_bf16, oracle_weights,
+                             rel_fro, row_scales, run_stages, small_case, weights_from)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,8 @@ def check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, H, I):
     assert np.array_equal(bf16_to_np(st["xg"])[:R], xg)
     xq, xsf = O.quantize_rows(xg, offs)
     assert np.array_equal(st["xq"][:R].cpu().numpy(), xq)
-    assert np.array_equal(st["xsf"][:xsf.size].cpu().numpy(), xsf)
+    want = chunk32_bytes(row_scales(xsf, offs, H), offs, H)
+    assert np.array_equal(st["xsf"][:want.size].cpu().numpy(), want)
     d13 = O.grouped_gemm(xq, xsf, offs, gexp, w_np["w13_packed"], w_np["w13_sf_linear"])
     assert rel_fro(st["d13"][:R].cpu().numpy(), d13) <= GEMM_TOL
     h_ref = O.swiglu(st["d13"][:R].cpu().numpy().astype(np.float64), offs, gexp, w_np["g_gate_up"])
@@ -64,7 +65,8 @@ def check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, H, I):
     h_gpu = bf16_to_np(st["h"])[:R]
     hq, hsf = O.quantize_rows(h_gpu, offs)
     assert np.array_equal(st["hq"][:R].cpu().numpy(), hq)
-    assert np.array_equal(st["hsf"][:hsf.size].cpu().numpy(), hsf)
+    want = chunk32_bytes(row_scales(hsf, offs, I), offs, I)
+    assert np.array_equal(st["hsf"][:want.size].cpu().numpy(), want)
     d2 = O.grouped_gemm(hq, hsf, offs, gexp, w_np["w2_packed"], w_np["w2_sf_linear"])
     assert rel_fro(st["d2"][:R].cpu().numpy(), d2) <= GEMM_TOL
     y_ref = O.scatter_add(st["d2"][:R].cpu().numpy().astype(np.float64), row_slot, ids_np, tw_np,
@@ -184,18 +186,22 @@ def edge_rows(R, K, seed=0):
     return np.asarray(O.f64_to_bf16_bits(x.astype(np.float64)))
 
 
-@pytest.mark.parametrize("mg,K", [((1, 130), 64), ((3, 17, 1, 140), 256), ((1,), 4096)])
+@pytest.mark.parametrize("mg,K", [((1, 130), 64), ((3, 17, 1, 140), 256), ((1,), 4096), ((33, 64, 5), 1024)])
 def test_quantize_rows_bit_exact(cuda, mg, K):
+    """Both token-scale layouts, every byte (padding included) against the
+    oracle; 0xAB fill shows that every byte of the region is written."""
     R = sum(mg)
     rows = edge_rows(R, K, seed=R + K)
     _, G = _groups_for(mg, cuda)
     offs = np.concatenate([[0], np.cumsum(mg)])
-    packed = torch.zeros(R, K // 2, dtype=torch.uint8, device=cuda)
-    sf = torch.full((N.sf_bytes(R, len(mg), K),), 0xAB, dtype=torch.uint8, device=cuda)
-    N.nvfp4_quantize_rows(np_to_bf16(rows, cuda), G, packed, sf)
     ref_p, ref_sf = O.quantize_rows(rows, offs)
-    assert np.array_equal(packed.cpu().numpy(), ref_p)
-    assert np.array_equal(sf[:ref_sf.size].cpu().numpy(), ref_sf)
+    for layout in (N.SF_ATOM128, N.SF_CHUNK32):
+        packed = torch.zeros(R, K // 2, dtype=torch.uint8, device=cuda)
+        sf = torch.full((N.sf_bytes(R, len(mg), K, layout),), 0xAB, dtype=torch.uint8, device=cuda)
+        N.nvfp4_quantize_rows(np_to_bf16(rows, cuda), G, packed, sf, layout)
+        assert np.array_equal(packed.cpu().numpy(), ref_p)
+        want = ref_sf if layout == N.SF_ATOM128 else chunk32_bytes(row_scales(ref_sf, offs, K), offs, K)
+        assert np.array_equal(sf[:want.size].cpu().numpy(), want), layout
     if mg == (1, 130):
         assert ref_p.nbytes + ref_sf.nbytes == 5728
 
@@ -208,12 +214,13 @@ def test_gather_quantize_fused_equals_separate(cuda):
     G = N.Groups(T, k, E, cuda)
     xg = torch.zeros(S, H, dtype=torch.bfloat16, device=cuda)
     N.moe_gather_rows(x, ids, E, G, xg)
-    p1 = torch.zeros(S, H // 2, dtype=torch.uint8, device=cuda)
-    s1 = torch.zeros(N.sf_bytes(S, E, H), dtype=torch.uint8, device=cuda)
-    p2, s2 = p1.clone(), s1.clone()
-    N.nvfp4_quantize_rows(xg, G, p1, s1)
-    N.moe_gather_quantize_rows(x, k, G, p2, s2)
-    assert torch.equal(p1, p2) and torch.equal(s1, s2)
+    for layout in (N.SF_ATOM128, N.SF_CHUNK32):
+        p1 = torch.zeros(S, H // 2, dtype=torch.uint8, device=cuda)
+        s1 = torch.zeros(N.sf_bytes(S, E, H, layout), dtype=torch.uint8, device=cuda)
+        p2, s2 = p1.clone(), s1.clone()
+        N.nvfp4_quantize_rows(xg, G, p1, s1, layout)
+        N.moe_gather_quantize_rows(x, k, G, p2, s2, layout)
+        assert torch.equal(p1, p2) and torch.equal(s1, s2)
 
 
 # ---------------------------------------------------------------------------
