@@ -34,7 +34,7 @@ design notes of the repository):
   * rows of a group ascend by slot index t*k + j; groups ascend by expert id.
   * GEMM outputs are fp32 on the device (fp64 here), h and y are bf16.
   * expert ids outside [0, E) mark unused slots.
-Parity pins for every function live in tests/test_oracle_*.py.
+Parity pins for every function live in tests/oracle_pins.py (run by tests/test_oracle.py).
 """
 from __future__ import annotations
 
