@@ -213,6 +213,28 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
                     const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
                     void* workspace, size_t ws_bytes, uint16_t* y, cudaStream_t stream);
 
+/* moe_nvfp4_layer_static -- moe_nvfp4_layer without a workspace argument,
+ * for callers that cannot allocate device memory: a plugin or kernel library
+ * whose host owns every allocation, code that must not synchronize the device
+ * (cudaMalloc/cudaFree can), or a caller that builds the step into work it
+ * does not own. The pages have no counterpart; it exists for such callers.
+ * The workspace is one device array inside the library of
+ * MOE_NVFP4_STATIC_SCRATCH_BYTES (8 MiB), held by every GPU that loads the
+ * library until the process exits. Sizes whose
+ * moe_nvfp4_layer_workspace_size() exceeds it return MOE_ERR_WORKSPACE (at
+ * H = 4096, I = 2048, E = 288 that allows T*k <= 64, i.e. decode up to 8
+ * streams of top-8). Nothing is allocated: the first call on a device looks up
+ * the array's device address once (make that first call before any stream
+ * capture); no part of the array needs to start at zero, every byte the step
+ * reads is written earlier in the same call. All calls share the one array:
+ * calls that can overlap on the GPU (different streams, or the same stream
+ * from several host threads without ordering) race and must be serialized by
+ * the caller. Arguments and results otherwise as moe_nvfp4_layer. */
+#define MOE_NVFP4_STATIC_SCRATCH_BYTES (8u << 20)
+int moe_nvfp4_layer_static(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
+                           const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
+                           uint16_t* y, cudaStream_t stream);
+
 /* Load-time helper (not part of the timed step): weight tiling for the
  * grouped GEMM. packed [rows, K/2] e2m1 and linear scales [rows, K/16] ->
  * `tiled` (nvfp4_tiled_bytes(rows, K) bytes): for each 128-row tile and each

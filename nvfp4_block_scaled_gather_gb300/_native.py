@@ -57,6 +57,8 @@ _SIGS = {
     "moe_nvfp4_layer": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                 ctypes.POINTER(MoeWeights), c_void_p, c_size_t, c_void_p, c_void_p]),
     "nvfp4_swizzle_block_scales": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
+    "moe_nvfp4_layer_static": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
+                                       ctypes.POINTER(MoeWeights), c_void_p, c_void_p]),
     "nvfp4_tiled_bytes": (c_size_t, [c_int, c_int]),
     "nvfp4_tile_weights": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p]),
 }
@@ -255,6 +257,20 @@ def moe_nvfp4_layer(x, topk_ids, topk_w, weights: Weights, workspace, y, stream=
            load().moe_nvfp4_layer(_ptr(x), T, H, weights.I, _ptr(topk_ids), _ptr(topk_w), k,
                                   ctypes.byref(weights.struct), _ptr(workspace), workspace.numel(), _ptr(y),
                                   _stream(stream)))
+
+
+STATIC_SCRATCH_BYTES = 8 << 20  # MOE_NVFP4_STATIC_SCRATCH_BYTES
+
+
+def moe_nvfp4_layer_static(x, topk_ids, topk_w, weights: Weights, y, stream=None):
+    """The layer step with the library's own fixed scratch array instead of a
+    caller workspace, for callers that may not allocate device memory. Calls
+    that can overlap on the GPU share that array and must be serialized."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_nvfp4_layer_static",
+           load().moe_nvfp4_layer_static(_ptr(x), T, H, weights.I, _ptr(topk_ids), _ptr(topk_w), k,
+                                         ctypes.byref(weights.struct), _ptr(y), _stream(stream)))
 
 
 class MoeLayer:
