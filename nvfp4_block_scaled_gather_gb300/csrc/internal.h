@@ -44,21 +44,30 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
                             const moe_groups_t& g, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
 // h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
-cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
-                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf,
-                          cudaStream_t s);
+// d13 holds nparts partial products part_stride floats apart, added in order.
+cudaError_t launch_swiglu(const float* d13, int nparts, size_t part_stride, int R_max, int E, int I,
+                          const moe_groups_t& g, int layout, const float* g_gate_up, uint16_t* h, uint8_t* packed,
+                          uint8_t* sf, cudaStream_t s);
 // Load-time weight tiling for the grouped GEMM (rows % 128 == 0).
 cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
                         cudaStream_t s);
 inline size_t tiled_bytes(long long rows, long long K) { return (size_t)(rows / 128) * ((K + 255) / 256) * 18432; }
-cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w,
-                           int T, int k, int E, const moe_groups_t& g, const float* g_down,
+cudaError_t launch_scatter(const float* d2, int nparts, size_t part_stride, int H, const int32_t* topk_ids,
+                           const float* topk_w, int T, int k, int E, const moe_groups_t& g, const float* g_down,
                            uint16_t* y, cudaStream_t s);
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s);
 
 // tcgen05 grouped GEMM (nvfp4_gemm.cu). status: device word for wait timeouts.
+// part_stride == 0: d gets the finished product. part_stride > 0: the K loop
+// is split into gemm_segments(K) work items and segment s's partial goes to
+// d + s * part_stride; the consumer adds them in segment order, which gives
+// the same bits as the finished product.
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf,
                                 const moe_groups_t& g, int R_max, const uint8_t* w_tiled, int E, int N,
-                                int K, float* d, int* status, cudaStream_t s);
+                                int K, float* d, size_t part_stride, int* status, cudaStream_t s);
+int gemm_segments(int K);  // fixed 1024-value accumulation segments of a K-long dot product
+// Split the GEMMs of a layer when its work units are few (decode): a function
+// of the sizes only, so a row's result never depends on the batch.
+inline bool split_gemms(long long S, long long E, long long N) { return chunks_bound(S, E) * (N / 128) <= 2048; }
 
 }  // namespace moe

@@ -55,6 +55,8 @@ struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
   float *d13, *d2;
+  int parts13, parts2;            // K-segment partials per GEMM output (1: finished product)
+  size_t stride13, stride2;       // floats between partials (0 when not split)
   size_t bytes;
 };
 
@@ -72,10 +74,15 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
   w.xsf = take(token_sf_bytes((long long)S, E, H, MOE_SF_CHUNK32));
-  w.d13 = reinterpret_cast<float*>(take(S * 2 * I * sizeof(float)));
+  const bool split13 = split_gemms((long long)S, E, 2LL * I), split2 = split_gemms((long long)S, E, H);
+  w.parts13 = split13 ? gemm_segments(H) : 1;
+  w.parts2 = split2 ? gemm_segments(I) : 1;
+  w.stride13 = split13 ? S * 2 * I : 0;
+  w.stride2 = split2 ? S * H : 0;
+  w.d13 = reinterpret_cast<float*>(take((size_t)w.parts13 * S * 2 * I * sizeof(float)));
   w.hq = take(S * I / 2);
   w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
-  w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
+  w.d2 = reinterpret_cast<float*>(take((size_t)w.parts2 * S * H * sizeof(float)));
   w.bytes = off;
   return w;
 }
@@ -198,7 +205,7 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
     return MOE_ERR_INVALID;
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, st, stream));
+  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, 0, st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -207,7 +214,8 @@ int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
+  return status_of(
+      launch_swiglu(d13, 1, 0, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
 }
 
 int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, int layout,
@@ -217,7 +225,7 @@ int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
+  return status_of(launch_swiglu(d13, 1, 0, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
 }
 
 int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k, int E,
@@ -227,7 +235,7 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
   if (T == 0) return MOE_OK;
   if (!y || (k > 0 && (!d2 || !topk_ids || !topk_w || !g_down))) return MOE_ERR_INVALID;
   if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
-  return status_of(launch_scatter(d2, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
+  return status_of(launch_scatter(d2, 1, 0, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
 }
 
 size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I) {
@@ -258,12 +266,15 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
   if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, st, stream);
+    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, ws.stride13, st,
+                              stream);
   if (err == cudaSuccess)
-    err = launch_swiglu(ws.d13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, nullptr, ws.hq, ws.hsf, stream);
+    err = launch_swiglu(ws.d13, ws.parts13, ws.stride13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, nullptr,
+                        ws.hq, ws.hsf, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, st, stream);
-  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, ws.stride2, st, stream);
+  if (err == cudaSuccess)
+    err = launch_scatter(ws.d2, ws.parts2, ws.stride2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
 }
 

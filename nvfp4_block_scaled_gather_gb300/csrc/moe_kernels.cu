@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
 // a5 (+ a6) SwiGLU with per-group gate/up globals; same grid as the quantizer
 // over the I-wide output. Each lane reads 4 gate and 4 up fp32 values.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int I, moe_groups_t g,
+__global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int nparts,
+                                                          size_t part_stride, int I, moe_groups_t g,
                                                           int layout, const float* __restrict__ g_gate_up,
                                                           uint16_t* __restrict__ h, uint8_t* __restrict__ packed,
                                                           uint8_t* __restrict__ sf) {
@@ -308,8 +309,16 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
     const int r = rb.row0 + m;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + kc0 + 4 * q));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(d13 + (size_t)r * 2 * I + I + kc0 + 4 * q));
+      // gate and up: the partial products of the w13 GEMM added in segment order
+      const float* src = d13 + (size_t)r * 2 * I + kc0 + 4 * q;
+      float4 a = __ldg(reinterpret_cast<const float4*>(src));
+      float4 b = __ldg(reinterpret_cast<const float4*>(src + I));
+      for (int pi = 1; pi < nparts; ++pi) {
+        const float4 a2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride));
+        const float4 b2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride + I));
+        a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+        b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+      }
       const float ga[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int z = 0; z < 4; ++z) {
@@ -338,7 +347,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
 // token's used slots by grouped row (ascending expert), then every thread
 // accumulates 4 columns in that order in fp32.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restrict__ d2, int H,
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restrict__ d2, int nparts,
+                                                           size_t part_stride, int H,
                                                            const int32_t* __restrict__ ids,
                                                            const float* __restrict__ topk_w, int k, int E,
                                                            moe_groups_t g, const float* __restrict__ g_down,
@@ -372,7 +382,12 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
   const int n = s_n;
   for (int i = 0; i < n; ++i) {
     const float c = s_coef[i];
-    const float4 d = __ldg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i] * H + col));
+    const float* src = d2 + (size_t)s_row[i] * H + col;
+    float4 d = __ldg(reinterpret_cast<const float4*>(src));
+    for (int pi = 1; pi < nparts; ++pi) {  // w2 partial products, in segment order
+      const float4 d_2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride));
+      d.x += d_2.x; d.y += d_2.y; d.z += d_2.z; d.w += d_2.w;
+    }
     a0 = __fmaf_rn(c, d.x, a0);
     a1 = __fmaf_rn(c, d.y, a1);
     a2 = __fmaf_rn(c, d.z, a2);
@@ -470,10 +485,11 @@ cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
-                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
+cudaError_t launch_swiglu(const float* d13, int nparts, size_t part_stride, int R_max, int E, int I,
+                          const moe_groups_t& g, int layout, const float* g_gate_up, uint16_t* h, uint8_t* packed,
+                          uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (I + kColsPerCta - 1) / kColsPerCta);
-  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, I, g, layout, g_gate_up, h, packed, sf);
+  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, nparts, part_stride, I, g, layout, g_gate_up, h, packed, sf);
   return cudaGetLastError();
 }
 
@@ -485,10 +501,11 @@ cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int row
   return cudaGetLastError();
 }
 
-cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k,
-                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s) {
+cudaError_t launch_scatter(const float* d2, int nparts, size_t part_stride, int H, const int32_t* topk_ids,
+                           const float* topk_w, int T, int k, int E, const moe_groups_t& g, const float* g_down,
+                           uint16_t* y, cudaStream_t s) {
   dim3 grid(T, (H + kThreads * 4 - 1) / (kThreads * 4));
-  scatter_kernel<<<grid, kThreads, 0, s>>>(d2, H, topk_ids, topk_w, k, E, g, g_down, y);
+  scatter_kernel<<<grid, kThreads, 0, s>>>(d2, nparts, part_stride, H, topk_ids, topk_w, k, E, g, g_down, y);
   return cudaGetLastError();
 }
 

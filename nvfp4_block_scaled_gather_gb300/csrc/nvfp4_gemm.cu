@@ -53,6 +53,7 @@ constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
 constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
 constexpr int kBBoxRows = 16;
 constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
+constexpr int kSegStages = 4;       // K stages per accumulation segment (1024 values)
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
 constexpr int kCtasPerSm = 2;
@@ -70,6 +71,8 @@ struct GemmArgs {
   const int32_t* group_chunk;
   int* status;
   int N, K;
+  int split;              // 1: one work item per K-segment, partials to d + seg * part_stride
+  size_t part_stride;     // floats between segment partials (split only)
   long long wait_budget;  // clock64 cycles a single wait may take
 };
 
@@ -294,17 +297,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t tmem_base = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.wait_budget};
 
+  // Work items: a whole unit, or (p.split) one K-segment of a unit. Every
+  // segment (kSegStages stages) accumulates from zero in TMEM; a unit's result
+  // is the fp32 sum of its segments in segment order, formed either here (the
+  // epilogue's running sum) or by the consumer from the stored partials. The
+  // two give identical bits, so splitting is a scheduling choice only.
+  const int nseg = (nk + kSegStages - 1) / kSegStages;
+  const int per_unit = p.split ? nseg : 1;
+  const int total_items = total_units * per_unit;
+
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if (lane == 0 && total_units > 0) {
+    if (lane == 0 && total_items > 0) {
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
       const uint64_t stream_policy = policy_evict_first();
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
+        const int u = it / per_unit;
+        const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
         const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
         const int nbox = un.nmma / kBBoxRows;
-        for (int ks = 0; ks < nk; ++ks) {
+        const int ks_end = min(nk, seg1 * kSegStages);
+        for (int ks = seg0 * kSegStages; ks < ks_end; ++ks) {
           if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
@@ -335,38 +350,44 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == 1) {
     // ============================= MMA issuer =============================
-    if (lane == 0 && total_units > 0) {
+    if (lane == 0 && total_items > 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
+        const int u = it / per_unit;
+        const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
         const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
-        if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
         const uint32_t idesc = idesc_nvf4(un.nmma);
-        for (int ks = 0; ks < nk; ++ks) {
-          if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
+        for (int sg = seg0; ok && sg < seg1; ++sg) {
+          if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
           tc_fence_after();
-          const int natoms = min(4, kc4 - 4 * ks);
-          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
-          const uint32_t sWs = sW + stage * kWStageBytes;
-          for (int a = 0; a < natoms; ++a) {
-            tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
-            tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
+          const int ks0 = sg * kSegStages, ks_end = min(nk, ks0 + kSegStages);
+          for (int ks = ks0; ks < ks_end; ++ks) {
+            if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const int natoms = min(4, kc4 - 4 * ks);
+            const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+            const uint32_t sWs = sW + stage * kWStageBytes;
+            for (int a = 0; a < natoms; ++a) {
+              tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
+              tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
+            }
+            for (int a = 0; a < natoms; ++a) {
+              const uint64_t adesc = desc_sw128(sWs + 32 * a);
+              const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
+              tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a,
+                          (ks != ks0 || a != 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
+            if (++stage == stages) { stage = 0; phase ^= 1u; }
           }
-          for (int a = 0; a < natoms; ++a) {
-            const uint64_t adesc = desc_sw128(sWs + 32 * a);
-            const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
-          }
-          tc_commit(empty_bar(stage));
-          if (++stage == stages) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          tc_commit(accf_bar(acc));
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
         }
-        if (!ok) break;
-        tc_commit(accf_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) {
         // wait for every MMA / scale copy issued so far before TMEM is freed
@@ -381,33 +402,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
+      const int u = it / per_unit;
+      const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
       const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
-      if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
-      tc_fence_after();
       const int n = un.nt * kBM + quad * 32 + lane;
-      float* dcol = p.d + (size_t)un.row0 * p.N + n;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
-      // one load of 16 or 32 columns from the buffer's first column (aligned)
-      if (un.nvalid <= 16) {
-        uint32_t r[16];
-        tc_ld_32x32b_x16(taddr, r);
+      float sum[kTokChunk];
+      for (int sg = seg0; sg < seg1; ++sg) {
+        if (!wait_phase(accf_bar(acc), acc_phase, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
+        uint32_t r[kTokChunk];
+        // one load of 16 or 32 columns from the buffer's first column (aligned)
+        if (un.nvalid <= 16) {
+          tc_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+          tc_ld_32x32b_x32(taddr, r);
+        }
         tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(acce_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        if (p.split) {
+          float* dst = p.d + (size_t)sg * p.part_stride + (size_t)un.row0 * p.N + n;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < un.nvalid) dcol[(size_t)j * p.N] = __uint_as_float(r[j]);
-      } else {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(taddr, r);
-        tc_wait_ld();
+          for (int j = 0; j < kTokChunk; ++j)
+            if (j < un.nvalid) dst[(size_t)j * p.N] = __uint_as_float(r[j]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < un.nvalid) dcol[(size_t)j * p.N] = __uint_as_float(r[j]);
+          for (int j = 0; j < kTokChunk; ++j) sum[j] = sg == 0 ? __uint_as_float(r[j]) : sum[j] + __uint_as_float(r[j]);
+          if (sg == nseg - 1) {
+            float* dst = p.d + (size_t)un.row0 * p.N + n;
+#pragma unroll
+            for (int j = 0; j < kTokChunk; ++j)
+              if (j < un.nvalid) dst[(size_t)j * p.N] = sum[j];
+          }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(acce_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
   __syncwarp();
@@ -448,8 +481,11 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
 
 }  // namespace
 
+int gemm_segments(int K) { return ((K + 255) / 256 + kSegStages - 1) / kSegStages; }
+
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
-                                const uint8_t* w_tiled, int E, int N, int K, float* d, int* status, cudaStream_t s) {
+                                const uint8_t* w_tiled, int E, int N, int K, float* d, size_t part_stride,
+                                int* status, cudaStream_t s) {
   CUtensorMap tmB;
   if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
   GemmArgs p;
@@ -464,6 +500,8 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
   p.status = status;
   p.N = N;
   p.K = K;
+  p.split = part_stride > 0 ? 1 : 0;
+  p.part_stride = part_stride;
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
@@ -471,7 +509,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
                                (int)cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
   const long long chunks_bound = (long long)(E < R_max ? E : R_max) + (R_max + kTokChunk - 1) / kTokChunk;
-  const long long units_bound = chunks_bound * (N / kBM);
+  const long long units_bound = chunks_bound * (N / kBM) * (part_stride > 0 ? gemm_segments(K) : 1);
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
   gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmB, p);
