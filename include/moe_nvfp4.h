@@ -86,6 +86,8 @@ enum { MOE_SF_ATOM128 = 0, MOE_SF_CHUNK32 = 1 };
  *   group_expert[E]      expert id of group g (ascending)
  *   group_sf_block[E+1]  first 128-row scale block of group g; entry G = total
  *   group_chunk[E+1]     first 32-row GEMM chunk of group g; entry G = total
+ *   chunk_info[4*C]      per 32-row chunk c: first grouped row, rows (1..32),
+ *                        expert id, group; C = min(E, T*k) + ceil(T*k/32)
  *   row_slot[T*k]        slot t*k+j of grouped row r (r < R)
  *   slot_row[T*k]        grouped row of slot s, or -1 for an unused slot     */
 typedef struct {
@@ -94,6 +96,7 @@ typedef struct {
   int32_t* group_expert;
   int32_t* group_sf_block;
   int32_t* group_chunk;
+  int32_t* chunk_info;
   int32_t* row_slot;
   int32_t* slot_row;
 } moe_groups_t;

@@ -24,7 +24,7 @@ SF_CHUNK32 = 1   # per 32-row chunk, the layout nvfp4_grouped_gemm reads
 
 class MoeGroups(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("counts", "group_offsets", "group_expert", "group_sf_block",
-                                       "group_chunk", "row_slot", "slot_row")]
+                                       "group_chunk", "chunk_info", "row_slot", "slot_row")]
 
 
 class MoeWeights(ctypes.Structure):
@@ -133,6 +133,7 @@ class Groups:
                     group_expert=self.view("group_expert", G).cpu(),
                     group_sf_block=self.view("group_sf_block", G + 1).cpu(),
                     group_chunk=self.view("group_chunk", G + 1).cpu(),
+                    chunk_info=self.view("chunk_info", 4 * nchunk).cpu().reshape(-1, 4),
                     row_slot=self.view("row_slot", R).cpu(),
                     slot_row=self.view("slot_row", S).cpu())
 

@@ -62,9 +62,12 @@ cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzle
 // is split into gemm_segments(K) work items and segment s's partial goes to
 // d + s * part_stride; the consumer adds them in segment order, which gives
 // the same bits as the finished product.
+// early: the group metadata and the weights were written two or more
+// launches back (true inside moe_nvfp4_layer), so the GEMM may read them and
+// start streaming weights before the previous kernel has finished.
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf,
                                 const moe_groups_t& g, int R_max, const uint8_t* w_tiled, int E, int N,
-                                int K, float* d, size_t part_stride, int* status, cudaStream_t s);
+                                int K, float* d, size_t part_stride, bool early, int* status, cudaStream_t s);
 int gemm_segments(int K);  // fixed 1024-value accumulation segments of a K-long dot product
 // Split the GEMMs of a layer when its work units are few (decode): a function
 // of the sizes only, so a row's result never depends on the batch.

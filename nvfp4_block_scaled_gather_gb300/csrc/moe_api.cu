@@ -44,7 +44,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool groups_ok(const moe_groups_t* g) {
   return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->group_chunk &&
-         g->row_slot && g->slot_row;
+         g->chunk_info && g->row_slot && g->slot_row;
 }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -133,7 +133,8 @@ size_t moe_groups_bytes(int T, int k, int E) {
   if (T < 0 || k < 0 || E < 0) return 0;
   const size_t S = (size_t)T * k;
   return align256(16 * 4) + align256(4 * (size_t)(E + 1)) + align256(4 * (size_t)E) +
-         2 * align256(4 * (size_t)(E + 1)) + 2 * align256(4 * S);
+         2 * align256(4 * (size_t)(E + 1)) + align256(16 * (size_t)chunks_bound((long long)S, E)) +
+         2 * align256(4 * S);
 }
 
 int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
@@ -146,6 +147,7 @@ int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
   g->group_expert = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)E);
   g->group_sf_block = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
   g->group_chunk = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
+  g->chunk_info = reinterpret_cast<int32_t*>(p); p += align256(16 * (size_t)chunks_bound((long long)S, E));
   g->row_slot = reinterpret_cast<int32_t*>(p); p += align256(4 * S);
   g->slot_row = reinterpret_cast<int32_t*>(p);
   return MOE_OK;
@@ -205,7 +207,7 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
     return MOE_ERR_INVALID;
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, 0, st, stream));
+  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, 0, false, st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -266,13 +268,14 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
   if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, ws.stride13, st,
-                              stream);
+    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, ws.stride13, true,
+                              st, stream);
   if (err == cudaSuccess)
     err = launch_swiglu(ws.d13, ws.parts13, ws.stride13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, nullptr,
                         ws.hq, ws.hsf, stream);
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, ws.stride2, st, stream);
+    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, ws.stride2, true, st,
+                              stream);
   if (err == cudaSuccess)
     err = launch_scatter(ws.d2, ws.parts2, ws.stride2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);

@@ -16,6 +16,7 @@
 
 #include "internal.h"
 #include "nvfp4_codec.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -41,6 +42,8 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__ ids, int S, int E,
                                                      moe_groups_t g) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   extern __shared__ int32_t smem[];
   int32_t* wc = smem;                // [32][E]: counts, then running row cursors
   int32_t* rowbase = smem + 32 * E;  // [E]: first row of each expert
@@ -107,6 +110,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
       g.group_offsets[gi] = row0;
       g.group_sf_block[gi] = blk0;
       g.group_chunk[gi] = chk0;
+      for (int q = 0; q < own3; ++q)  // the group's 32-row chunks
+        reinterpret_cast<int4*>(g.chunk_info)[chk0 + q] = make_int4(row0 + 32 * q, min(32, cnt - 32 * q), tid, gi);
     }
   }
   if (tid == 0) {
@@ -150,6 +155,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                           moe_groups_t g, uint16_t* __restrict__ xg) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   const int R = __ldg(g.counts + 1);
   const int per_row = H / 8;
   const long long total = (long long)R * per_row;
@@ -212,24 +219,26 @@ struct ScaleTarget {
 };
 
 // The CTA's row block `blk` (128 rows per block in the atom layout, 32 in the
-// chunk layout): first grouped row, valid rows and group.
+// chunk layout): first grouped row, valid rows and expert.
 struct RowBlock {
-  int row0, nvalid, gi;
+  int row0, nvalid, expert;
 };
 
 __device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int layout, int blk) {
+  if (layout == MOE_SF_CHUNK32) {  // one table read, same value in every thread
+    const int4 c = __ldg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
+    return RowBlock{c.x, c.y, c.z};
+  }
   __shared__ int s_info[3];
   if (threadIdx.x == 0) {
     const int G = __ldg(g.counts + 0);
-    const int32_t* starts = layout == MOE_SF_ATOM128 ? g.group_sf_block : g.group_chunk;
-    const int rows = layout == MOE_SF_ATOM128 ? kRowsAtom : kRowsChunk;
-    const int gi = find_group(starts, G, blk);
-    const int m0 = (blk - __ldg(starts + gi)) * rows;
+    const int gi = find_group(g.group_sf_block, G, blk);
+    const int m0 = (blk - __ldg(g.group_sf_block + gi)) * kRowsAtom;
     const int r0 = __ldg(g.group_offsets + gi);
     const int mg = __ldg(g.group_offsets + gi + 1) - r0;
     s_info[0] = r0 + m0;
-    s_info[1] = min(rows, mg - m0);
-    s_info[2] = gi;
+    s_info[1] = min(kRowsAtom, mg - m0);
+    s_info[2] = __ldg(g.group_expert + gi);
   }
   __syncthreads();
   return RowBlock{s_info[0], s_info[1], s_info[2]};
@@ -249,6 +258,8 @@ constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K)
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k, int K,
                                                             moe_groups_t g, int layout, uint8_t* __restrict__ packed,
                                                             uint8_t* __restrict__ sf) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   const int blk = blockIdx.x;
   if (blk >= routed_blocks(g, layout)) return;
   const RowBlock rb = resolve_block(g, layout, blk);
@@ -289,10 +300,12 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
                                                           int layout, const float* __restrict__ g_gate_up,
                                                           uint16_t* __restrict__ h, uint8_t* __restrict__ packed,
                                                           uint8_t* __restrict__ sf) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   const int blk = blockIdx.x;
   if (blk >= routed_blocks(g, layout)) return;
   const RowBlock rb = resolve_block(g, layout, blk);
-  const int e = __ldg(g.group_expert + rb.gi);
+  const int e = rb.expert;
   const float gg = __ldg(g_gate_up + 2 * e), gu = __ldg(g_gate_up + 2 * e + 1);
   const int Kc = I / 16;
   const int kc0 = blockIdx.y * kColsPerCta;
@@ -353,6 +366,8 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
                                                            const float* __restrict__ topk_w, int k, int E,
                                                            moe_groups_t g, const float* __restrict__ g_down,
                                                            uint16_t* __restrict__ y) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_coef[kMaxTopK];
   __shared__ int s_n;
@@ -406,6 +421,8 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) swizzle_kernel(const uint8_t* __restrict__ linear, int N, int Kc,
                                                            uint8_t* __restrict__ out) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   const int Np = (N + 127) / 128 * 128;
   const int words = Kc / 4;
   const long long total = (long long)Np * words;
@@ -427,6 +444,8 @@ __global__ void __launch_bounds__(kThreads) swizzle_kernel(const uint8_t* __rest
 __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restrict__ packed,
                                                         const uint8_t* __restrict__ sf_linear, int tiles, int K,
                                                         uint8_t* __restrict__ out) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
   const int nk = (K + 255) / 256, rowb = K / 2, Kc = K / 16;
   const long long chunks = (long long)tiles * nk * 128 * 8;
   const long long words = (long long)tiles * nk * 4 * 128;
@@ -468,51 +487,46 @@ cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups
     cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  route_kernel<<<1, 1024, smem, s>>>(topk_ids, S, E, g);
-  return cudaGetLastError();
+  return launch_pdl(route_kernel, dim3(1), dim3(1024), smem, s, topk_ids, S, E, g);
 }
 
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g, uint16_t* xg,
                           cudaStream_t s) {
-  gather_kernel<<<grid_for((long long)R_max * (H / 8)), kThreads, 0, s>>>(x, H, k, g, xg);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(grid_for((long long)R_max * (H / 8))), dim3(kThreads), 0, s, x, H, k, g, xg);
 }
 
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K, const moe_groups_t& g,
                             int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kColsPerCta - 1) / kColsPerCta);
-  quantize_kernel<<<grid, kThreads, 0, s>>>(src, src_k, K, g, layout, packed, sf);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel, grid, dim3(kThreads), 0, s, src, src_k, K, g, layout, packed, sf);
 }
 
 cudaError_t launch_swiglu(const float* d13, int nparts, size_t part_stride, int R_max, int E, int I,
                           const moe_groups_t& g, int layout, const float* g_gate_up, uint16_t* h, uint8_t* packed,
                           uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (I + kColsPerCta - 1) / kColsPerCta);
-  swiglu_kernel<<<grid, kThreads, 0, s>>>(d13, nparts, part_stride, I, g, layout, g_gate_up, h, packed, sf);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_kernel, grid, dim3(kThreads), 0, s, d13, nparts, part_stride, I, g, layout, g_gate_up, h,
+                    packed, sf);
 }
 
 cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
                         cudaStream_t s) {
   const long long tiles = rows / 128, nk = (K + 255) / 256;
   const long long items = tiles * nk * (128 * 8 + 4 * 128);
-  tile_kernel<<<grid_for(items), kThreads, 0, s>>>(packed, sf_linear, (int)tiles, K, tiled);
-  return cudaGetLastError();
+  return launch_pdl(tile_kernel, dim3(grid_for(items)), dim3(kThreads), 0, s, packed, sf_linear, (int)tiles, K, tiled);
 }
 
 cudaError_t launch_scatter(const float* d2, int nparts, size_t part_stride, int H, const int32_t* topk_ids,
                            const float* topk_w, int T, int k, int E, const moe_groups_t& g, const float* g_down,
                            uint16_t* y, cudaStream_t s) {
   dim3 grid(T, (H + kThreads * 4 - 1) / (kThreads * 4));
-  scatter_kernel<<<grid, kThreads, 0, s>>>(d2, nparts, part_stride, H, topk_ids, topk_w, k, E, g, g_down, y);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, grid, dim3(kThreads), 0, s, d2, nparts, part_stride, H, topk_ids, topk_w, k, E, g,
+                    g_down, y);
 }
 
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s) {
   const long long items = (long long)((N + 127) / 128 * 128) * (K / 64);
-  swizzle_kernel<<<grid_for(items), kThreads, 0, s>>>(linear, N, K / 16, swizzled);
-  return cudaGetLastError();
+  return launch_pdl(swizzle_kernel, dim3(grid_for(items)), dim3(kThreads), 0, s, linear, N, K / 16, swizzled);
 }
 
 }  // namespace moe

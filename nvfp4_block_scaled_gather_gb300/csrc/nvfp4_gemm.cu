@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -69,9 +70,11 @@ struct GemmArgs {
   const int32_t* group_expert;
   const int32_t* group_sf_block;
   const int32_t* group_chunk;
+  const int32_t* chunk_info;
   int* status;
   int N, K;
   int split;              // 1: one work item per K-segment, partials to d + seg * part_stride
+  int early;              // 1: group metadata and weights were written two or more launches back
   size_t part_stride;     // floats between segment partials (split only)
   long long wait_budget;  // clock64 cycles a single wait may take
 };
@@ -85,6 +88,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -200,15 +206,6 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl
   }
 }
 
-__device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, int G, int key) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(starts + mid) <= key) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // One unit of work: 32-row chunk `chunk` of a group (its rows [32q, 32q+32))
 // against 128-row weight tile `nt` of the group's expert. The chunk's token
 // scales are one 512-byte block per K-atom (layout MOE_SF_CHUNK32), copied to
@@ -218,20 +215,17 @@ struct Unit {
   size_t w_off, sfb_off;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int G, int kc4, int nk) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int nk) {
   const int chunk = u / n_tiles;
   Unit un;
   un.nt = u - chunk * n_tiles;
-  const int gi = find_group(p.group_chunk, G, chunk);
-  const int q = chunk - __ldg(p.group_chunk + gi);
-  const int r0 = __ldg(p.group_offsets + gi);
-  const int mg = __ldg(p.group_offsets + gi + 1) - r0;
-  const int e = __ldg(p.group_expert + gi);
-  un.row0 = r0 + kTokChunk * q;
-  un.nvalid = min(kTokChunk, mg - kTokChunk * q);
+  const int4 c = __ldg(reinterpret_cast<const int4*>(p.chunk_info) + chunk);  // row0, rows, expert, group
+  const int e = c.z;
+  un.row0 = c.x;
+  un.nvalid = c.y;
   un.nmma = (un.nvalid + 15) & ~15;
   un.w_off = ((size_t)e * n_tiles + un.nt) * nk * kWStageBytes;
-  un.sfb_off = (size_t)chunk * kc4 * kAtomBytes;
+  un.sfb_off = (size_t)chunk * (p.K / 64) * kAtomBytes;
   return un;
 }
 
@@ -251,6 +245,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel in the stream still runs. Everything it reads must be complete
+  // first; with p.early the group metadata and the weights are two or more
+  // launches old (complete), and only the token operand waits below.
+  if (!p.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // ---- schedule shape, identical on every thread ----
   const int G = __ldg(p.counts + 0);
@@ -308,26 +310,64 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == 0) {
     // ============================ TMA producer ============================
+    if (lane == 0 && total_items == 0 && p.early) {
+      pdl_wait();
+      pdl_trigger();
+    }
     if (lane == 0 && total_items > 0) {
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
       const uint64_t stream_policy = policy_evict_first();
+      // With p.early, the weight copies of the first ring slots go out before
+      // waiting for the previous kernel (they do not depend on it); the token
+      // rows and their scales follow once it has completed.
+      int prefetched = 0;
+      if (p.early) {
+        int it = blockIdx.x, ks = -1, ks_end = 0;
+        const Unit* unp = nullptr;
+        Unit un;
+        for (int slot = 0; slot < stages; ++slot) {
+          if (++ks >= ks_end) {  // next work item
+            if (unp) it += gridDim.x;
+            if (it >= total_items) break;
+            const int u = it / per_unit;
+            const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
+            un = decode_unit(u, p, n_tiles, nk);
+            unp = &un;
+            ks = seg0 * kSegStages;
+            ks_end = min(nk, seg1 * kSegStages);
+          }
+          const int natoms = min(4, kc4 - 4 * ks);
+          const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
+          mbar_expect_tx_only(full_bar(slot), wbytes);
+          bulk_load_hint(sW + slot * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes,
+                         full_bar(slot), stream_policy);
+          ++prefetched;
+        }
+        pdl_wait();
+        pdl_trigger();
+      }
+      int issued = 0;
       for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
         const int u = it / per_unit;
         const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
-        const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
+        const Unit un = decode_unit(u, p, n_tiles, nk);
         const int nbox = un.nmma / kBBoxRows;
         const int ks_end = min(nk, seg1 * kSegStages);
-        for (int ks = seg0 * kSegStages; ks < ks_end; ++ks) {
-          if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
+        for (int ks = seg0 * kSegStages; ks < ks_end; ++ks, ++issued) {
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
-          const uint32_t bytes = wbytes + nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
+          const uint32_t tbytes = nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
           const uint32_t fb = full_bar(stage);
-          mbar_expect_tx(fb, bytes);
-          bulk_load_hint(sW + stage * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes, fb,
-                         stream_policy);
+          if (issued < prefetched) {
+            mbar_expect_tx(fb, tbytes);  // weights already on their way
+          } else {
+            if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
+            mbar_expect_tx(fb, wbytes + tbytes);
+            bulk_load_hint(sW + stage * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes, fb,
+                           stream_policy);
+          }
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, &tmB, ks * kStageKBytes,
                         un.row0 + b * kBBoxRows, fb);
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
         const int u = it / per_unit;
         const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
-        const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
+        const Unit un = decode_unit(u, p, n_tiles, nk);
         const uint32_t idesc = idesc_nvf4(un.nmma);
         for (int sg = seg0; ok && sg < seg1; ++sg) {
           if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
@@ -406,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
       const int u = it / per_unit;
       const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
-      const Unit un = decode_unit(u, p, n_tiles, G, kc4, nk);
+      const Unit un = decode_unit(u, p, n_tiles, nk);
       const int n = un.nt * kBM + quad * 32 + lane;
       float sum[kTokChunk];
       for (int sg = seg0; sg < seg1; ++sg) {
@@ -485,7 +525,7 @@ int gemm_segments(int K) { return ((K + 255) / 256 + kSegStages - 1) / kSegStage
 
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
                                 const uint8_t* w_tiled, int E, int N, int K, float* d, size_t part_stride,
-                                int* status, cudaStream_t s) {
+                                bool early, int* status, cudaStream_t s) {
   CUtensorMap tmB;
   if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
   GemmArgs p;
@@ -497,10 +537,12 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
   p.group_expert = g.group_expert;
   p.group_sf_block = g.group_sf_block;
   p.group_chunk = g.group_chunk;
+  p.chunk_info = g.chunk_info;
   p.status = status;
   p.N = N;
   p.K = K;
   p.split = part_stride > 0 ? 1 : 0;
+  p.early = early ? 1 : 0;
   p.part_stride = part_stride;
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -512,8 +554,7 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
   const long long units_bound = chunks_bound * (N / kBM) * (part_stride > 0 ? gemm_segments(K) : 1);
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
-  gemm_kernel<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(tmB, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, tmB, p);
 }
 
 }  // namespace moe

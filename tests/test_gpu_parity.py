@@ -39,6 +39,9 @@ def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
     assert np.array_equal(host["group_sf_block"].numpy(), O.group_sf_blocks(ref_offs))
     chunks = np.concatenate([[0], np.cumsum((np.diff(ref_offs) + 31) // 32)])
     assert np.array_equal(host["group_chunk"].numpy(), chunks) and host["chunks"] == chunks[-1]
+    info = [(ref_offs[g] + 32 * q, min(32, ref_offs[g + 1] - ref_offs[g] - 32 * q), ref_gexp[g], g)
+            for g in range(G) for q in range(chunks[g + 1] - chunks[g])]
+    assert np.array_equal(host["chunk_info"].numpy(), np.array(info, dtype=np.int64).reshape(-1, 4))
     assert host["max_mg"] == (int(np.diff(ref_offs).max()) if G else 0)
     slot_row = np.full(S, -1)
     slot_row[ref_row_slot] = np.arange(len(ref_row_slot))
