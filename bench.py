@@ -163,6 +163,7 @@ def gpu_bench(args, rank, world):
                   w["g_down"])
     del w
     flush = torch.empty(2 * props.L2_cache_size, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(2 * props.L2_cache_size // 4, dtype=torch.int32, device=dev)
 
     def workload(c, n=N_ROUTINGS):
         items = []
@@ -176,21 +177,35 @@ def gpu_bench(args, rank, world):
                               R=int(valid.numel())))
         return items
 
-    def time_layer(c, items, steps, warmup, sampler=None):
+    def flush_l2():
+        """Write a buffer twice the L2, then read another: the weights leave
+        L2 and the lines left behind are clean (no write-backs in the step)."""
+        flush.zero_()
+        flush_read.sum(dtype=torch.int32)
+
+    def time_layer(c, items, steps, warmup, sampler=None, graph=True):
+        """Times `steps` layer steps (mean and per-step CUDA events), L2
+        flushed before each. graph=True replays one CUDA graph per routing
+        (captured from the same C-ABI call); graph=False calls it directly."""
         T_max = max(it["T"] for it in items)
         layer = N.MoeLayer(W, T_max, c.k)
         ys = [torch.empty_like(it["x"]) for it in items]
+        if graph:
+            graphs = [layer.capture(it["x"], it["ids"], it["tw"], y) for it, y in zip(items, ys)]
+            run = lambda i: graphs[i % len(items)].replay()  # noqa: E731
+        else:
+            def run(i):
+                it = items[i % len(items)]
+                layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
         for i in range(warmup):
-            it = items[i % len(items)]
-            layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+            run(i)
         if sampler is not None:
             # keep the clocks sampler busy for at least ~1 s of load before timing
             t0 = time.time()
             i = 0
             while time.time() - t0 < 1.0:
-                it = items[i % len(items)]
-                flush.zero_()
-                layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+                flush_l2()
+                run(i)
                 i += 1
                 if i % 20 == 0:
                     torch.cuda.synchronize()
@@ -199,10 +214,9 @@ def gpu_bench(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
         for i in range(steps):
-            it = items[i % len(items)]
-            flush.zero_()
+            flush_l2()
             ev[i][0].record(stream)
-            layer(it["x"], it["ids"], it["tw"], ys[i % len(items)])
+            run(i)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         if dist:
@@ -231,7 +245,7 @@ def gpu_bench(args, rank, world):
             T = it["T"]
             G1 = N.Groups(T, c.k, c.E, dev) if T != T_max else G_
             y = torch.empty_like(it["x"])
-            flush.zero_()
+            flush_l2()
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
             evs[0].record(stream)
             N.moe_route_groups(it["ids"], c.E, G1)
@@ -255,32 +269,38 @@ def gpu_bench(args, rank, world):
 
     def time_e2e(c, items, steps):
         """Through the public call with host buffers: pinned H2D of x, ids and
-        router weights, the layer, D2H of y; all inside the timed region."""
+        router weights into the layer's input buffers, the layer step (its
+        captured graph), D2H of y; all inside the timed region."""
         T_max = max(it["T"] for it in items)
         layer = N.MoeLayer(W, T_max, c.k)
-        host = []
+        host, dev_bufs, graphs = [], [], []
         for it in items:
             host.append(dict(x=it["x"].cpu().pin_memory(), ids=it["ids_h"].pin_memory(),
                              tw=it["tw_h"].pin_memory(), y=torch.empty_like(it["x"], device="cpu").pin_memory(),
                              T=it["T"], G=it["G"]))
+            d = dict(x=torch.empty_like(it["x"]), ids=torch.empty_like(it["ids"]), tw=torch.empty_like(it["tw"]),
+                     y=torch.empty_like(it["x"]))
+            d["x"].copy_(it["x"]), d["ids"].copy_(it["ids"]), d["tw"].copy_(it["tw"])
+            graphs.append(layer.capture(d["x"], d["ids"], d["tw"], d["y"]))
+            dev_bufs.append(d)
         ms, h2d, d2h, byts = [], [], [], []
         for i in range(steps + 3):
-            h = host[i % len(host)]
-            flush.zero_()
+            h, d = host[i % len(host)], dev_bufs[i % len(host)]
+            flush_l2()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            x = h["x"].to(dev, non_blocking=True)
-            ids = h["ids"].to(dev, non_blocking=True)
-            tw = h["tw"].to(dev, non_blocking=True)
-            y = layer(x, ids, tw)
-            h["y"].copy_(y, non_blocking=True)
+            d["x"].copy_(h["x"], non_blocking=True)
+            d["ids"].copy_(h["ids"], non_blocking=True)
+            d["tw"].copy_(h["tw"], non_blocking=True)
+            graphs[i % len(host)].replay()
+            h["y"].copy_(d["y"], non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
             if i >= 3:
                 ms.append(e0.elapsed_time(e1))
-                h2d.append(x.numel() * 2 + ids.numel() * 4 + tw.numel() * 4)
-                d2h.append(y.numel() * 2)
+                h2d.append(d["x"].numel() * 2 + d["ids"].numel() * 4 + d["tw"].numel() * 4)
+                d2h.append(d["y"].numel() * 2)
                 byts.append(step_bytes(c, h["G"], h["T"]))
         return ms, byts, statistics.mean(h2d), statistics.mean(d2h)
 
@@ -291,13 +311,14 @@ def gpu_bench(args, rank, world):
     items = workload(cfg)
     if args.profile:
         # short run for profilers: warm-up, then the timed steps, nothing else
-        ms, byts = time_layer(cfg, items, args.steps, args.warmup)
+        ms, byts = time_layer(cfg, items, args.steps, args.warmup, graph=False)
         print(json.dumps({"profile_run": cfg.name, "experts": cfg.E, "ms_per_step": statistics.mean(ms)}))
         return
     sampler = ClockSampler(gpu_id)
     sampler.wait_first()
-    ms, byts = time_layer(cfg, items, args.steps, args.warmup, sampler)
+    ms, byts = time_layer(cfg, items, args.steps, args.warmup, sampler, graph=not args.eager)
     clocks = sampler.stop()
+    ms_eager, _ = time_layer(cfg, items, max(10, min(args.steps, 40)), 3, graph=False)
     if dist:
         t = torch.tensor([sum(ms)], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -320,7 +341,7 @@ def gpu_bench(args, rank, world):
                 continue
             c = CONFIGS[name]
             it2 = workload(c)
-            m2, b2 = time_layer(c, it2, max(10, min(args.steps, 40)), 3)
+            m2, b2 = time_layer(c, it2, max(10, min(args.steps, 40)), 3, graph=not args.eager)
             g2 = sum(b2) / (sum(m2) * 1e-3) / 1e9
             per_config[name] = {"ms_per_step": round(statistics.mean(m2), 5), "weight_gbs": round(g2, 1),
                                 "roof_frac": round(g2 / peak, 4),
@@ -336,6 +357,8 @@ def gpu_bench(args, rank, world):
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
         "ms_per_step_median": round(statistics.median(ms), 5),
+        "step_launch": "eager C-ABI call" if args.eager else "CUDA graph of the C-ABI call (one per routing buffer set)",
+        "ms_per_step_eager": round(statistics.mean(ms_eager), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -348,7 +371,8 @@ def gpu_bench(args, rank, world):
             "mean_active_experts": statistics.mean(i["G"] for i in items),
             "rows_per_step": statistics.mean(i["R"] for i in items),
             "bytes_per_step": statistics.mean(byts),
-            "l2": "flushed before every timed step (write of 2x L2); routing rotated over 20 seeded draws",
+            "l2": "flushed before every timed step (write of a 2x-L2 buffer, then a read of another); "
+                  "routing rotated over 20 seeded draws",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roof_frac": round(gbs / world / peak, 4),
@@ -516,6 +540,7 @@ def main():
                     help="further configs timed on one GPU and reported under per_config")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--profile", action="store_true", help="short run for ncu: warm-up and timed steps only")
+    ap.add_argument("--eager", action="store_true", help="time direct calls instead of CUDA-graph replays")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
