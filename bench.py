@@ -47,10 +47,11 @@ def step_bytes(cfg, G, T):
 
 
 def w13_launch_bytes(cfg, G, R):
-    """Algorithmic bytes of one w13 grouped-GEMM launch: the active experts'
-    w13 (2I x H e2m1 + scales), the NVFP4 activation rows and their scales,
-    the fp32 output rows."""
-    return G * 2 * cfg.I * cfg.H * 9 // 16 + R * cfg.H * 9 // 16 + R * 2 * cfg.I * 4
+    """Algorithmic bytes of one w13 grouped-GEMM launch (SwiGLU and the
+    requantization fused in its epilogue): the active experts' w13 (2I x H
+    e2m1 + scales), the NVFP4 activation rows and their scales, the NVFP4
+    h rows and their scales."""
+    return G * 2 * cfg.I * cfg.H * 9 // 16 + R * cfg.H * 9 // 16 + R * cfg.I * 9 // 16
 
 
 def measured_peaks():
@@ -233,11 +234,10 @@ def gpu_bench(args, rank, world):
         G_ = N.Groups(T_max, c.k, c.E, dev)
         xq = torch.empty(S, c.H // 2, dtype=torch.uint8, device=dev)
         xsf = torch.empty(N.sf_bytes(S, c.E, c.H, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
-        d13 = torch.empty(S, 2 * c.I, dtype=torch.float32, device=dev)
         hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
         hsf = torch.empty(N.sf_bytes(S, c.E, c.I, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
         d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
-        names = ["route", "gather_quantize", "gemm_w13", "swiglu_quantize", "gemm_w2", "scatter"]
+        names = ["route", "gather_quantize", "gemm_w13", "gemm_w2", "scatter"]
         acc = {n: [] for n in names}
         w13_bytes = []
         for i in range(steps + 3):
@@ -252,14 +252,12 @@ def gpu_bench(args, rank, world):
             evs[1].record(stream)
             N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf)
             evs[2].record(stream)
-            N.nvfp4_grouped_gemm(xq, xsf, G1, W.w13, d13)
+            N.nvfp4_grouped_gemm_swiglu(xq, xsf, G1, W.w13, W.g_gate_up, hq, hsf)
             evs[3].record(stream)
-            N.swiglu_quantize_grouped(d13, G1, W.g_gate_up, hq, hsf)
-            evs[4].record(stream)
             N.nvfp4_grouped_gemm(hq, hsf, G1, W.w2, d2)
-            evs[5].record(stream)
+            evs[4].record(stream)
             N.moe_scatter_add(d2, it["ids"], it["tw"], c.E, G1, W.g_down, y)
-            evs[6].record(stream)
+            evs[5].record(stream)
             torch.cuda.synchronize()
             if i >= 3:
                 for j, n in enumerate(names):

@@ -104,11 +104,13 @@ typedef struct {
 /* Expert weights (device), in the GEMM tiling made once at load time by
  * nvfp4_tile_weights from packed e2m1 [E, N, K/2] and linear e4m3 scales
  * [E, N, K/16]. w13 rows 0..I-1 are gate, I..2I-1 are up, back to back (first
- * page, "The seam CUTLASS forced open": the pair doubles as the fused w13
- * operand; with I % 128 == 0 no tile straddles the two halves). */
+ * page, "The seam CUTLASS forced open": the pair is the fused w13 operand);
+ * w13 is tiled with interleave_rows = 2I, so every 128-row tile holds 64 gate
+ * rows and the matching 64 up rows and the SwiGLU of a tile is formed in the
+ * GEMM's epilogue. w2 is tiled plainly (interleave_rows = 0). */
 typedef struct {
   int E;
-  const uint8_t* w13_tiled;   /* nvfp4_tiled_bytes(E*2I, H) bytes: w13 [E, 2I, H] */
+  const uint8_t* w13_tiled;   /* nvfp4_tiled_bytes(E*2I, H) bytes: w13 [E, 2I, H], interleaved */
   const float* g_gate_up;     /* [E, 2]: gate global, up global */
   const uint8_t* w2_tiled;    /* nvfp4_tiled_bytes(E*H, I) bytes: w2 [E, H, I] */
   const float* g_down;        /* [E] */
@@ -167,17 +169,31 @@ int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, cons
 /* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
  * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
  * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
- * a_sf is in MOE_SF_CHUNK32. W [E, N, K] comes tiled by nvfp4_tile_weights.
- * A group larger than 32 rows is processed as ceil(Mg/32) chunks, each
- * streaming the expert's weights (decode groups hold at most a few dozen
- * rows). One launch for all groups on
+ * a_sf is in MOE_SF_CHUNK32. W [E, N, K] comes tiled by nvfp4_tile_weights;
+ * w_interleaved says it was tiled with interleave_rows = N (columns of d are
+ * in natural order either way). A group larger than 32 rows is processed as
+ * ceil(Mg/32) chunks, each streaming the expert's weights (decode groups hold
+ * at most a few dozen rows). One launch for all groups on
  * tcgen05 block-scaled MMA (kind::mxf4nvf4, scale vector 16), accumulators in
  * tensor memory. First page, "What changed": grouped GEMM w13 N=4096 K=4096
  * and w2 N=4096 K=2048, alpha = 1. N % 128 == 0, K % 64 == 0; every pointer
  * 16-byte aligned. */
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
-                       int R_max, const uint8_t* w_tiled, int E, int N, int K, float* d,
+                       int R_max, const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
                        cudaStream_t stream);
+
+/* a4 + a5 + a6 fused -- the w13 grouped GEMM with SwiGLU and requantization
+ * in its epilogue: from the NVFP4 rows (a_sf in MOE_SF_CHUNK32) and w13 tiled
+ * with interleave_rows = 2I, writes NVFP4 h: packed [R_max, I/2] and token
+ * scales h_sf (MOE_SF_CHUNK32, nvfp4_sf_bytes(R_max, E, I, 1) bytes). The
+ * fp32 gate|up product never leaves the chip. Bit-identical to
+ * nvfp4_grouped_gemm + swiglu_grouped + nvfp4_quantize_rows. The second
+ * page's "SwiGLU as an epilogue" found this inexpressible in CUTLASS grouped
+ * GEMM; per-half globals are still applied in registers (option (a)).
+ * I % 128 == 0, K % 64 == 0. */
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
+                              int R_max, const uint8_t* w13_tiled, int E, int I, int K, const float* g_gate_up,
+                              uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream);
 
 /* a5 -- swiglu_grouped: h[r, n] = silu(d13[r, n]*g_gate[e]) * (d13[r, I+n]*g_up[e]),
  * computed in fp32 (CUDA expf) and rounded once to bf16. d13 [R_max, 2I]
@@ -208,7 +224,9 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
 size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I);
 
 /* The whole step a1..a8 on `stream`: route-group, gather+quantize, grouped
- * GEMM w13, SwiGLU+requantize, grouped GEMM w2, scatter-add. x [T, H] bf16,
+ * GEMM w13 with SwiGLU+requantize in its epilogue, grouped GEMM w2,
+ * scatter-add (four kernels, each allowed to start while the previous one
+ * finishes: programmatic dependent launch). x [T, H] bf16,
  * y [T, H] bf16 (overwritten). `workspace` is caller device memory of
  * ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I), 256-byte
  * aligned. H % 128 == 0, I % 128 == 0, k <= 32, E <= 1024. */
@@ -247,11 +265,13 @@ int moe_nvfp4_layer_static(const uint16_t* x, int T, int H, int I, const int32_t
  * are zero. Same bytes as the inputs (up to the K padding), reordered so that
  * each stage is one contiguous read. Like the first page's load-time scale
  * swizzle ("The seam CUTLASS forced open"), it is paid once per weight, not
- * per step. For stacked experts pass rows = E*N. rows % 128 == 0,
- * K % 64 == 0. */
+ * per step. For stacked experts pass rows = E*N. interleave_rows = 0 keeps
+ * row order; interleave_rows = N (rows per expert, a multiple of 256) makes
+ * tile t of an expert hold its rows 64t..64t+63 and N/2+64t..N/2+64t+63.
+ * rows % 128 == 0, K % 64 == 0. */
 size_t nvfp4_tiled_bytes(int rows, int K);
-int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
-                       cudaStream_t stream);
+int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, int interleave_rows,
+                       uint8_t* tiled, cudaStream_t stream);
 
 /* Load-time helper (not part of the timed step): linear row-major scales
  * [N, K/16] -> the atom layout, N padded up to a multiple of 128 with zero

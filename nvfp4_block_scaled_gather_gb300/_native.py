@@ -46,7 +46,9 @@ _SIGS = {
     "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
                                          c_void_p, c_void_p, c_void_p]),
     "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int, c_int,
-                                   c_int, c_void_p, c_void_p]),
+                                   c_int, c_int, c_void_p, c_void_p]),
+    "nvfp4_grouped_gemm_swiglu": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int,
+                                          c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
                                c_void_p]),
     "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
@@ -60,7 +62,7 @@ _SIGS = {
     "moe_nvfp4_layer_static": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                        ctypes.POINTER(MoeWeights), c_void_p, c_void_p]),
     "nvfp4_tiled_bytes": (c_size_t, [c_int, c_int]),
-    "nvfp4_tile_weights": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p]),
+    "nvfp4_tile_weights": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
 }
 
 
@@ -174,17 +176,20 @@ def moe_gather_quantize_rows(x, k: int, groups: Groups, packed, sf, layout: int 
 
 
 class TiledWeight:
-    """One projection of all experts, [E, N, K], tiled for the grouped GEMM."""
+    """One projection of all experts, [E, N, K], tiled for the grouped GEMM.
+    interleave=True pairs rows of the two halves of N in every tile (the w13
+    gate|up layout the fused SwiGLU epilogue reads)."""
 
-    def __init__(self, packed, sf_linear, stream=None):
+    def __init__(self, packed, sf_linear, interleave: bool = False, stream=None):
         import torch
         self.E, self.N, K2 = packed.shape
         self.K = 2 * K2
+        self.interleaved = interleave
         rows = self.E * self.N
         self.data = torch.empty(load().nvfp4_tiled_bytes(rows, self.K), dtype=torch.uint8, device=packed.device)
         _check("nvfp4_tile_weights",
                load().nvfp4_tile_weights(_ptr(packed.contiguous()), _ptr(sf_linear.contiguous()), rows, self.K,
-                                         _ptr(self.data), _stream(stream)))
+                                         self.N if interleave else 0, _ptr(self.data), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w: TiledWeight, d, stream=None):
@@ -193,7 +198,18 @@ def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w: TiledWeight, d, stream
     assert K == w.K
     _check("nvfp4_grouped_gemm",
            load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max, _ptr(w.data),
-                                     w.E, w.N, K, _ptr(d), _stream(stream)))
+                                     int(w.interleaved), w.E, w.N, K, _ptr(d), _stream(stream)))
+
+
+def nvfp4_grouped_gemm_swiglu(a_packed, a_sf, groups: Groups, w13: TiledWeight, g_gate_up, h_packed, h_sf,
+                              stream=None):
+    R_max = a_packed.shape[0]
+    K = a_packed.shape[1] * 2
+    assert K == w13.K and w13.interleaved
+    _check("nvfp4_grouped_gemm_swiglu",
+           load().nvfp4_grouped_gemm_swiglu(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max,
+                                            _ptr(w13.data), w13.E, w13.N // 2, K, _ptr(g_gate_up), _ptr(h_packed),
+                                            _ptr(h_sf), _stream(stream)))
 
 
 def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):
@@ -239,8 +255,8 @@ class Weights:
         import torch
         self.E, I2, H2 = w13_packed.shape
         self.H, self.I = H2 * 2, I2 // 2
-        self.w13 = TiledWeight(w13_packed, w13_sf_linear, stream)
-        self.w2 = TiledWeight(w2_packed, w2_sf_linear, stream)
+        self.w13 = TiledWeight(w13_packed, w13_sf_linear, interleave=True, stream=stream)
+        self.w2 = TiledWeight(w2_packed, w2_sf_linear, stream=stream)
         self.g_gate_up = g_gate_up.to(torch.float32).contiguous()
         self.g_down = g_down.to(torch.float32).contiguous()
         self.struct = MoeWeights(self.E, self.w13.data.data_ptr(), self.g_gate_up.data_ptr(),

@@ -44,33 +44,36 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
                             const moe_groups_t& g, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
 // h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
-// d13 holds nparts partial products part_stride floats apart, added in order.
-cudaError_t launch_swiglu(const float* d13, int nparts, size_t part_stride, int R_max, int E, int I,
-                          const moe_groups_t& g, int layout, const float* g_gate_up, uint16_t* h, uint8_t* packed,
-                          uint8_t* sf, cudaStream_t s);
-// Load-time weight tiling for the grouped GEMM (rows % 128 == 0).
-cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
-                        cudaStream_t s);
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
+                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s);
+// Load-time weight tiling for the grouped GEMM (rows % 128 == 0). With
+// interleave_rows > 0 (rows per expert, a multiple of 256) each tile takes 64
+// rows of an expert's first half and the matching 64 of its second half.
+cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, int interleave_rows,
+                        uint8_t* tiled, cudaStream_t s);
 inline size_t tiled_bytes(long long rows, long long K) { return (size_t)(rows / 128) * ((K + 255) / 256) * 18432; }
-cudaError_t launch_scatter(const float* d2, int nparts, size_t part_stride, int H, const int32_t* topk_ids,
-                           const float* topk_w, int T, int k, int E, const moe_groups_t& g, const float* g_down,
-                           uint16_t* y, cudaStream_t s);
+cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k,
+                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s);
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s);
 
 // tcgen05 grouped GEMM (nvfp4_gemm.cu). status: device word for wait timeouts.
-// part_stride == 0: d gets the finished product. part_stride > 0: the K loop
-// is split into gemm_segments(K) work items and segment s's partial goes to
-// d + s * part_stride; the consumer adds them in segment order, which gives
-// the same bits as the finished product.
+// w_interleaved: each 128-row weight tile holds 64 rows of the first half of
+// N and the matching 64 rows of the second half (nvfp4_tile_weights with
+// interleave). swiglu == nullptr: d gets fp32 rows in natural column order.
+// swiglu != nullptr (needs w_interleaved, N = 2I): the epilogue applies
+// SwiGLU with the per-expert (gate, up) globals and writes NVFP4 h (packed
+// [R_max, I/2], token scales MOE_SF_CHUNK32), bit-identical to swiglu_grouped
+// followed by nvfp4_quantize_rows; d is not written.
 // early: the group metadata and the weights were written two or more
 // launches back (true inside moe_nvfp4_layer), so the GEMM may read them and
 // start streaming weights before the previous kernel has finished.
-cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf,
-                                const moe_groups_t& g, int R_max, const uint8_t* w_tiled, int E, int N,
-                                int K, float* d, size_t part_stride, bool early, int* status, cudaStream_t s);
-int gemm_segments(int K);  // fixed 1024-value accumulation segments of a K-long dot product
-// Split the GEMMs of a layer when its work units are few (decode): a function
-// of the sizes only, so a row's result never depends on the batch.
-inline bool split_gemms(long long S, long long E, long long N) { return chunks_bound(S, E) * (N / 128) <= 2048; }
+struct SwigluOut {
+  uint8_t* packed;
+  uint8_t* sf;
+  const float* g_gate_up;
+};
+cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
+                                const uint8_t* w_tiled, bool w_interleaved, int E, int N, int K, float* d,
+                                const SwigluOut* swiglu, bool early, int* status, cudaStream_t s);
 
 }  // namespace moe

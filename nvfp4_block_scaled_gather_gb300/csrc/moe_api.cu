@@ -54,9 +54,7 @@ bool layout_ok(int layout) { return layout == MOE_SF_ATOM128 || layout == MOE_SF
 struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
-  float *d13, *d2;
-  int parts13, parts2;            // K-segment partials per GEMM output (1: finished product)
-  size_t stride13, stride2;       // floats between partials (0 when not split)
+  float* d2;
   size_t bytes;
 };
 
@@ -74,15 +72,9 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
   w.xsf = take(token_sf_bytes((long long)S, E, H, MOE_SF_CHUNK32));
-  const bool split13 = split_gemms((long long)S, E, 2LL * I), split2 = split_gemms((long long)S, E, H);
-  w.parts13 = split13 ? gemm_segments(H) : 1;
-  w.parts2 = split2 ? gemm_segments(I) : 1;
-  w.stride13 = split13 ? S * 2 * I : 0;
-  w.stride2 = split2 ? S * H : 0;
-  w.d13 = reinterpret_cast<float*>(take((size_t)w.parts13 * S * 2 * I * sizeof(float)));
   w.hq = take(S * I / 2);
   w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
-  w.d2 = reinterpret_cast<float*>(take((size_t)w.parts2 * S * H * sizeof(float)));
+  w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
   w.bytes = off;
   return w;
 }
@@ -196,9 +188,10 @@ int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, cons
 }
 
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
-                       const uint8_t* w_tiled, int E, int N, int K, float* d, cudaStream_t stream) {
+                       const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
+                       cudaStream_t stream) {
   if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID;
-  if (N % 128 || K % 64) return MOE_ERR_SHAPE;
+  if (N % 128 || K % 64 || (w_interleaved && N % 256)) return MOE_ERR_SHAPE;
   if ((long long)E * N > (1LL << 31)) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!a_packed || !a_sf || !w_tiled || !d) return MOE_ERR_INVALID;
@@ -207,7 +200,27 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
     return MOE_ERR_INVALID;
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, E, N, K, d, 0, false, st, stream));
+  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, w_interleaved != 0, E, N, K, d,
+                                       nullptr, false, st, stream));
+}
+
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
+                              const uint8_t* w13_tiled, int E, int I, int K, const float* g_gate_up,
+                              uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || E <= 0 || I <= 0 || K <= 0) return MOE_ERR_INVALID;
+  if (I % 128 || K % 64) return MOE_ERR_SHAPE;
+  if ((long long)E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!a_packed || !a_sf || !w13_tiled || !g_gate_up || !h_packed || !h_sf) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(a_packed) % 16 || reinterpret_cast<uintptr_t>(w13_tiled) % 16 ||
+      reinterpret_cast<uintptr_t>(a_sf) % 16 || reinterpret_cast<uintptr_t>(h_packed) % 16 ||
+      reinterpret_cast<uintptr_t>(h_sf) % 16)
+    return MOE_ERR_INVALID;
+  int* st = status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  const SwigluOut out{h_packed, h_sf, g_gate_up};
+  return status_of(
+      launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w13_tiled, true, E, 2 * I, K, nullptr, &out, false, st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -216,8 +229,7 @@ int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
-  return status_of(
-      launch_swiglu(d13, 1, 0, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
 }
 
 int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, int layout,
@@ -227,7 +239,7 @@ int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
-  return status_of(launch_swiglu(d13, 1, 0, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
+  return status_of(launch_swiglu(d13, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
 }
 
 int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k, int E,
@@ -237,7 +249,7 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
   if (T == 0) return MOE_OK;
   if (!y || (k > 0 && (!d2 || !topk_ids || !topk_w || !g_down))) return MOE_ERR_INVALID;
   if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
-  return status_of(launch_scatter(d2, 1, 0, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
+  return status_of(launch_scatter(d2, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
 }
 
 size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I) {
@@ -267,17 +279,14 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   const int S = T * k;
   cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
   if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
+  const SwigluOut swiglu{ws.hq, ws.hsf, w->g_gate_up};  // a5 + a6 in the w13 GEMM's epilogue
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, E, 2 * I, H, ws.d13, ws.stride13, true,
+    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, true, E, 2 * I, H, nullptr, &swiglu, true,
                               st, stream);
   if (err == cudaSuccess)
-    err = launch_swiglu(ws.d13, ws.parts13, ws.stride13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, nullptr,
-                        ws.hq, ws.hsf, stream);
-  if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, E, H, I, ws.d2, ws.stride2, true, st,
+    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, false, E, H, I, ws.d2, nullptr, true, st,
                               stream);
-  if (err == cudaSuccess)
-    err = launch_scatter(ws.d2, ws.parts2, ws.stride2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
 }
 
@@ -286,16 +295,17 @@ size_t nvfp4_tiled_bytes(int rows, int K) {
   return tiled_bytes(rows, K);
 }
 
-int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
-                       cudaStream_t stream) {
-  if (rows < 0 || K <= 0) return MOE_ERR_INVALID;
+int nvfp4_tile_weights(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, int interleave_rows,
+                       uint8_t* tiled, cudaStream_t stream) {
+  if (rows < 0 || K <= 0 || interleave_rows < 0) return MOE_ERR_INVALID;
   if (rows % 128 || K % 64) return MOE_ERR_SHAPE;
+  if (interleave_rows > 0 && (interleave_rows % 256 || rows % interleave_rows)) return MOE_ERR_SHAPE;
   if (rows == 0) return MOE_OK;
   if (!packed || !sf_linear || !tiled) return MOE_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(packed) % 16 || reinterpret_cast<uintptr_t>(sf_linear) % 4 ||
       reinterpret_cast<uintptr_t>(tiled) % 16)
     return MOE_ERR_INVALID;
-  return status_of(launch_tile(packed, sf_linear, rows, K, tiled, stream));
+  return status_of(launch_tile(packed, sf_linear, rows, K, interleave_rows, tiled, stream));
 }
 
 int nvfp4_swizzle_block_scales(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t stream) {

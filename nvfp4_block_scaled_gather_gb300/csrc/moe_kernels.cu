@@ -295,8 +295,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
 // a5 (+ a6) SwiGLU with per-group gate/up globals; same grid as the quantizer
 // over the I-wide output. Each lane reads 4 gate and 4 up fp32 values.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int nparts,
-                                                          size_t part_stride, int I, moe_groups_t g,
+__global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restrict__ d13, int I, moe_groups_t g,
                                                           int layout, const float* __restrict__ g_gate_up,
                                                           uint16_t* __restrict__ h, uint8_t* __restrict__ packed,
                                                           uint8_t* __restrict__ sf) {
@@ -322,16 +321,9 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
     const int r = rb.row0 + m;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-      // gate and up: the partial products of the w13 GEMM added in segment order
       const float* src = d13 + (size_t)r * 2 * I + kc0 + 4 * q;
-      float4 a = __ldg(reinterpret_cast<const float4*>(src));
-      float4 b = __ldg(reinterpret_cast<const float4*>(src + I));
-      for (int pi = 1; pi < nparts; ++pi) {
-        const float4 a2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride));
-        const float4 b2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride + I));
-        a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
-        b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
-      }
+      const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(src + I));
       const float ga[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int z = 0; z < 4; ++z) {
@@ -360,8 +352,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
 // token's used slots by grouped row (ascending expert), then every thread
 // accumulates 4 columns in that order in fp32.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restrict__ d2, int nparts,
-                                                           size_t part_stride, int H,
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restrict__ d2, int H,
                                                            const int32_t* __restrict__ ids,
                                                            const float* __restrict__ topk_w, int k, int E,
                                                            moe_groups_t g, const float* __restrict__ g_down,
@@ -397,12 +388,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
   const int n = s_n;
   for (int i = 0; i < n; ++i) {
     const float c = s_coef[i];
-    const float* src = d2 + (size_t)s_row[i] * H + col;
-    float4 d = __ldg(reinterpret_cast<const float4*>(src));
-    for (int pi = 1; pi < nparts; ++pi) {  // w2 partial products, in segment order
-      const float4 d_2 = __ldg(reinterpret_cast<const float4*>(src + pi * part_stride));
-      d.x += d_2.x; d.y += d_2.y; d.z += d_2.z; d.w += d_2.w;
-    }
+    const float4 d = __ldg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i] * H + col));
     a0 = __fmaf_rn(c, d.x, a0);
     a1 = __fmaf_rn(c, d.y, a1);
     a2 = __fmaf_rn(c, d.z, a2);
@@ -439,11 +425,19 @@ __global__ void __launch_bounds__(kThreads) swizzle_kernel(const uint8_t* __rest
 // and 256-value K stage ks, an 18 KB block = 16 KB of e2m1 bytes in the
 // 128-byte-swizzled shared-memory image (16-byte chunk c of row r stored at
 // chunk c ^ (r % 8)) followed by the stage's four 512-byte scale atoms.
-// Values past K are zero.
+// Values past K are zero. With il > 0 (rows per expert), tile row j of an
+// expert's tile tt comes from row 64*tt + j (j < 64) or il/2 + 64*tt + j - 64.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ long long tile_src_row(int t, int j, int il) {
+  if (il <= 0) return (long long)t * 128 + j;
+  const int per = il / 128;  // tiles per expert
+  const long long e = t / per, tt = t - e * per;
+  return e * il + (j < 64 ? 64 * tt + j : il / 2 + 64 * tt + (j - 64));
+}
+
 __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restrict__ packed,
                                                         const uint8_t* __restrict__ sf_linear, int tiles, int K,
-                                                        uint8_t* __restrict__ out) {
+                                                        int il, uint8_t* __restrict__ out) {
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
   const int nk = (K + 255) / 256, rowb = K / 2, Kc = K / 16;
@@ -457,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restric
       const int ks = (int)(ts % nk), t = (int)(ts / nk);
       const int col = ks * 128 + c * 16;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (col < rowb) v = __ldg(reinterpret_cast<const uint4*>(packed + ((size_t)t * 128 + r) * rowb + col));
+      if (col < rowb) v = __ldg(reinterpret_cast<const uint4*>(packed + (size_t)tile_src_row(t, r, il) * rowb + col));
       *reinterpret_cast<uint4*>(out + (size_t)ts * 18432 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     } else {
       const long long j = i - chunks;
@@ -467,7 +461,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restric
       const int m = (wi >> 2) + 32 * (wi & 3);
       const int col = (4 * ks + a) * 4;  // first scale column of this atom
       uint32_t v = 0u;
-      if (col < Kc) v = __ldg(reinterpret_cast<const uint32_t*>(sf_linear + ((size_t)t * 128 + m) * Kc + col));
+      if (col < Kc) v = __ldg(reinterpret_cast<const uint32_t*>(sf_linear + (size_t)tile_src_row(t, m, il) * Kc + col));
       *reinterpret_cast<uint32_t*>(out + (size_t)ts * 18432 + 16384 + a * 512 + wi * 4) = v;
     }
   }
@@ -501,27 +495,24 @@ cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, in
   return launch_pdl(quantize_kernel, grid, dim3(kThreads), 0, s, src, src_k, K, g, layout, packed, sf);
 }
 
-cudaError_t launch_swiglu(const float* d13, int nparts, size_t part_stride, int R_max, int E, int I,
-                          const moe_groups_t& g, int layout, const float* g_gate_up, uint16_t* h, uint8_t* packed,
-                          uint8_t* sf, cudaStream_t s) {
+cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
+                          const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (I + kColsPerCta - 1) / kColsPerCta);
-  return launch_pdl(swiglu_kernel, grid, dim3(kThreads), 0, s, d13, nparts, part_stride, I, g, layout, g_gate_up, h,
-                    packed, sf);
+  return launch_pdl(swiglu_kernel, grid, dim3(kThreads), 0, s, d13, I, g, layout, g_gate_up, h, packed, sf);
 }
 
-cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, uint8_t* tiled,
-                        cudaStream_t s) {
+cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, int interleave_rows,
+                        uint8_t* tiled, cudaStream_t s) {
   const long long tiles = rows / 128, nk = (K + 255) / 256;
   const long long items = tiles * nk * (128 * 8 + 4 * 128);
-  return launch_pdl(tile_kernel, dim3(grid_for(items)), dim3(kThreads), 0, s, packed, sf_linear, (int)tiles, K, tiled);
+  return launch_pdl(tile_kernel, dim3(grid_for(items)), dim3(kThreads), 0, s, packed, sf_linear, (int)tiles, K,
+                    interleave_rows, tiled);
 }
 
-cudaError_t launch_scatter(const float* d2, int nparts, size_t part_stride, int H, const int32_t* topk_ids,
-                           const float* topk_w, int T, int k, int E, const moe_groups_t& g, const float* g_down,
-                           uint16_t* y, cudaStream_t s) {
+cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k,
+                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s) {
   dim3 grid(T, (H + kThreads * 4 - 1) / (kThreads * 4));
-  return launch_pdl(scatter_kernel, grid, dim3(kThreads), 0, s, d2, nparts, part_stride, H, topk_ids, topk_w, k, E, g,
-                    g_down, y);
+  return launch_pdl(scatter_kernel, grid, dim3(kThreads), 0, s, d2, H, topk_ids, topk_w, k, E, g, g_down, y);
 }
 
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s) {

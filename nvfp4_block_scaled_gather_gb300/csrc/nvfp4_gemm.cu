@@ -8,28 +8,31 @@
 // kernel with 128-row token tiles; this kernel is written for GB300 instead:
 //
 //  * Swap-AB. The weight tile is the MMA's A operand (M = 128 output features)
-//    and the group's tokens are the B operand (N = Mg rounded up to 16), so a
-//    decode group of one row costs a 16-wide MMA, not a 128-row tile. The
-//    second page ("Tiles below M=8") notes that the wasted token extent costs
-//    no HBM traffic; here it costs no tensor-core time either.
+//    and the group's tokens are the B operand (N = Mg rounded up to 16, at
+//    most 32 per unit), so a decode group of one row costs a 16-wide MMA, not
+//    a 128-row tile. The second page ("Tiles below M=8") notes that the wasted
+//    token extent costs no HBM traffic; here it costs no tensor work either.
 //  * Persistent CTAs, two per SM, walk the ragged work list of
 //    (32-token chunk of a group, 128-row weight tile) units in a fixed order;
 //    every unit streams its weight tile over the full K once. Two CTAs per SM
-//    because a CTA's tcgen05 ops (scale copies, MMAs) execute one after
-//    another: with one issuing CTA per SM the tensor pipe, not HBM, set the
-//    pace; two issuers overlap and the weight stream becomes HBM-bound.
+//    because a CTA's tcgen05 operations execute one after another: with one
+//    CTA per SM the tensor pipe, not HBM, set the pace.
 //  * Weights arrive pre-tiled (nvfp4_tile_weights, a load-time step): for
 //    every 128-row tile and 256-value K stage, 16 KB of e2m1 bytes already in
 //    the 128-byte-swizzled shared-memory image followed by the 2 KB of e4m3
-//    scale atoms. A stage is one contiguous 18 KB bulk copy, so each CTA
-//    streams its tile's weights sequentially from HBM (row-major tiles read
-//    128 bytes from each of 128 rows 2 KB apart, which left DRAM half idle).
+//    scale atoms, so a stage is one contiguous 18 KB bulk copy.
 //  * Warp roles: warp 0 issues the weight bulk copies (L2 evict-first), a TMA
 //    load of the token rows (128B-swizzled) and a bulk copy of their scale
-//    atoms into an mbarrier ring; warp 1
-//    copies scales into tensor memory (tcgen05.cp) and issues
-//    tcgen05.mma.kind::mxf4nvf4 (scale vector 16) into a double-buffered
-//    TMEM accumulator; warps 2-5 drain TMEM (tcgen05.ld) to fp32 global.
+//    atoms into an mbarrier ring; warp 6 copies each stage's scales into
+//    tensor memory (tcgen05.cp); warp 1 issues tcgen05.mma.kind::mxf4nvf4
+//    (scale vector 16) into a double-buffered TMEM accumulator; warps 2-5
+//    drain TMEM (tcgen05.ld).
+//  * Epilogue either writes fp32 rows, or (w13 in the layer) applies SwiGLU
+//    with the per-half globals and requantizes h to NVFP4 right there, so the
+//    fp32 gate|up product never reaches HBM. For that the w13 tiles hold 64
+//    gate rows and the matching 64 up rows (the first page's gate|up pair,
+//    "The seam CUTLASS forced open", reordered at load time); the pages could
+//    not express this epilogue in CUTLASS ("SwiGLU as an epilogue").
 //  * Every wait is bounded; on expiry the kernel records MOE_ERR_TIMEOUT,
 //    drains its own copies, frees tensor memory and returns.
 // A row's result never depends on other rows: the K loop order is fixed and
@@ -38,9 +41,11 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "nvfp4_codec.cuh"
 #include "pdl.cuh"
 
 namespace moe {
@@ -54,29 +59,30 @@ constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
 constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
 constexpr int kBBoxRows = 16;
 constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
-constexpr int kSegStages = 4;       // K stages per accumulation segment (1024 values)
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kThreads = 224;       // warp 0: TMA, 1: MMA, 2-5: epilogue, 6: scale copies
 constexpr int kCtasPerSm = 2;
 constexpr int kSmemBytes = 114688;  // per CTA: two CTAs fit the SM's 228 KB (1 KB reserved each)
 constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
+constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: up values [64][33] floats
+constexpr int kXchBytes = 9216;                    // 64 * 33 * 4 rounded up to 1 KB
 
 struct GemmArgs {
   const uint8_t* a_sf;
   const uint8_t* w_tiled;
-  float* d;
+  float* d;                 // plain epilogue: fp32 rows [R_max, N]
+  uint8_t* h_packed;        // fused epilogue: NVFP4 h [R_max, N/2 / 2] ...
+  uint8_t* h_sf;            // ... and its token scales (MOE_SF_CHUNK32, K = N/2)
+  const float* g_gate_up;   // ... with the per-expert (gate, up) globals
   const int32_t* counts;
-  const int32_t* group_offsets;
-  const int32_t* group_expert;
-  const int32_t* group_sf_block;
   const int32_t* group_chunk;
   const int32_t* chunk_info;
   int* status;
   int N, K;
-  int split;              // 1: one work item per K-segment, partials to d + seg * part_stride
-  int early;              // 1: group metadata and weights were written two or more launches back
-  size_t part_stride;     // floats between segment partials (split only)
-  long long wait_budget;  // clock64 cycles a single wait may take
+  int interleaved;          // tiles hold 64 gate rows then 64 up rows (halves of N)
+  int fused;                // 1: SwiGLU + requantize epilogue (needs interleaved)
+  int early;                // 1: group metadata and weights were written two or more launches back
+  long long wait_budget;    // clock64 cycles a single wait may take
 };
 
 // ------------------------------- PTX helpers --------------------------------
@@ -211,21 +217,21 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl
 // scales are one 512-byte block per K-atom (layout MOE_SF_CHUNK32), copied to
 // TMEM with tcgen05.cp.32x128b.warpx4 at a 4-column-aligned address.
 struct Unit {
-  int row0, nvalid, nmma, nt;
+  int chunk, row0, nvalid, nmma, nt, expert;
   size_t w_off, sfb_off;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int nk) {
-  const int chunk = u / n_tiles;
   Unit un;
-  un.nt = u - chunk * n_tiles;
-  const int4 c = __ldg(reinterpret_cast<const int4*>(p.chunk_info) + chunk);  // row0, rows, expert, group
-  const int e = c.z;
+  un.chunk = u / n_tiles;
+  un.nt = u - un.chunk * n_tiles;
+  const int4 c = __ldg(reinterpret_cast<const int4*>(p.chunk_info) + un.chunk);  // row0, rows, expert, group
   un.row0 = c.x;
   un.nvalid = c.y;
+  un.expert = c.z;
   un.nmma = (un.nvalid + 15) & ~15;
-  un.w_off = ((size_t)e * n_tiles + un.nt) * nk * kWStageBytes;
-  un.sfb_off = (size_t)chunk * (p.K / 64) * kAtomBytes;
+  un.w_off = ((size_t)un.expert * n_tiles + un.nt) * nk * kWStageBytes;
+  un.sfb_off = (size_t)un.chunk * (p.K / 64) * kAtomBytes;
   return un;
 }
 
@@ -234,13 +240,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain[1]
+  // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain, scales_ready[16], drain2,
+  // xch_full, xch_free
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+  auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStages + 5 + s); };
+  const uint32_t drain2_bar = bar0 + 8u * (3 * kMaxStages + 5);
+  const uint32_t xfull_bar = bar0 + 8u * (3 * kMaxStages + 6);
+  const uint32_t xfree_bar = bar0 + 8u * (3 * kMaxStages + 7);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
 
@@ -260,29 +271,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int nchunks = G > 0 ? __ldg(p.group_chunk + G) : 0;
   const int n_tiles = p.N / kBM;
   const int total_units = nchunks * n_tiles;
-  const int kc4 = p.K / 64;               // scale atoms along K per 128-row block
+  const int kc4 = p.K / 64;               // scale atoms along K per row block
   const int nk = (p.K + 255) / 256;       // stages per unit
   const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
   const int acc_cols = max(32, tn);
   const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
-  const int avail = kSmemBytes - 1024 - 1024;
+  const int avail = kSmemBytes - 1024 - 1024 - (p.fused ? kXchBytes : 0);
   int stages = min(kMaxStages, avail / stage_bytes);
   stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
-  // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, then token scales
+  // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, token scales, exchange
   const uint32_t sW = smem_u32(smem + 1024);
   const uint32_t sB = sW + (uint32_t)stages * kWStageBytes;
   const uint32_t sSFB = sB + (uint32_t)stages * tn * kStageKBytes;
+  float* xch = reinterpret_cast<float*>(smem + 1024 + (size_t)stages * stage_bytes);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sfr_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
       mbar_init(acce_bar(b), 4 * 32);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(drain2_bar, 1);
+    mbar_init(xfull_bar, 64);
+    mbar_init(xfree_bar, 64);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -299,22 +315,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t tmem_base = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.wait_budget};
 
-  // Work items: a whole unit, or (p.split) one K-segment of a unit. Every
-  // segment (kSegStages stages) accumulates from zero in TMEM; a unit's result
-  // is the fp32 sum of its segments in segment order, formed either here (the
-  // epilogue's running sum) or by the consumer from the stored partials. The
-  // two give identical bits, so splitting is a scheduling choice only.
-  const int nseg = (nk + kSegStages - 1) / kSegStages;
-  const int per_unit = p.split ? nseg : 1;
-  const int total_items = total_units * per_unit;
-
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if (lane == 0 && total_items == 0 && p.early) {
+    if (lane == 0 && total_units == 0 && p.early) {
       pdl_wait();
       pdl_trigger();
     }
-    if (lane == 0 && total_items > 0) {
+    if (lane == 0 && total_units > 0) {
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
@@ -324,38 +331,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // rows and their scales follow once it has completed.
       int prefetched = 0;
       if (p.early) {
-        int it = blockIdx.x, ks = -1, ks_end = 0;
-        const Unit* unp = nullptr;
-        Unit un;
-        for (int slot = 0; slot < stages; ++slot) {
-          if (++ks >= ks_end) {  // next work item
-            if (unp) it += gridDim.x;
-            if (it >= total_items) break;
-            const int u = it / per_unit;
-            const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
-            un = decode_unit(u, p, n_tiles, nk);
-            unp = &un;
-            ks = seg0 * kSegStages;
-            ks_end = min(nk, seg1 * kSegStages);
-          }
+        int u = blockIdx.x, ks = 0;
+        Unit un = decode_unit(u < total_units ? u : 0, p, n_tiles, nk);
+        for (int slot = 0; slot < stages && u < total_units; ++slot) {
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
           mbar_expect_tx_only(full_bar(slot), wbytes);
           bulk_load_hint(sW + slot * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes,
                          full_bar(slot), stream_policy);
           ++prefetched;
+          if (++ks == nk) {
+            ks = 0;
+            u += gridDim.x;
+            if (u < total_units) un = decode_unit(u, p, n_tiles, nk);
+          }
         }
         pdl_wait();
         pdl_trigger();
       }
       int issued = 0;
-      for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
-        const int u = it / per_unit;
-        const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const Unit un = decode_unit(u, p, n_tiles, nk);
         const int nbox = un.nmma / kBBoxRows;
-        const int ks_end = min(nk, seg1 * kSegStages);
-        for (int ks = seg0 * kSegStages; ks < ks_end; ++ks, ++issued) {
+        for (int ks = 0; ks < nk; ++ks, ++issued) {
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
           const uint32_t tbytes = nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
@@ -388,49 +386,74 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
       }
     }
-  } else if (warp == 1) {
-    // ============================= MMA issuer =============================
-    if (lane == 0 && total_items > 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+  } else if (warp == 6) {
+    // ======================== scale copies into TMEM =======================
+    // Stage slot s's scale columns are rewritten only after the slot was
+    // refilled, i.e. after the MMAs that read them completed (empty[s]).
+    if (lane == 0 && total_units > 0) {
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
-        const int u = it / per_unit;
-        const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
-        const Unit un = decode_unit(u, p, n_tiles, nk);
-        const uint32_t idesc = idesc_nvf4(un.nmma);
-        for (int sg = seg0; ok && sg < seg1; ++sg) {
-          if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
-          const int ks0 = sg * kSegStages, ks_end = min(nk, ks0 + kSegStages);
-          for (int ks = ks0; ks < ks_end; ++ks) {
-            if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const int natoms = min(4, kc4 - 4 * ks);
-            const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
-            const uint32_t sWs = sW + stage * kWStageBytes;
-            for (int a = 0; a < natoms; ++a) {
-              tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
-              tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
-            }
-            for (int a = 0; a < natoms; ++a) {
-              const uint64_t adesc = desc_sw128(sWs + 32 * a);
-              const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
-              tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a,
-                          (ks != ks0 || a != 0) ? 1u : 0u);
-            }
-            tc_commit(empty_bar(stage));
-            if (++stage == stages) { stage = 0; phase ^= 1u; }
+          const int natoms = min(4, kc4 - 4 * ks);
+          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+          const uint32_t sWs = sW + stage * kWStageBytes;
+          for (int a = 0; a < natoms; ++a) {
+            tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
+            tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
           }
-          if (!ok) break;
-          tc_commit(accf_bar(acc));
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
+          tc_commit(sfr_bar(stage));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
-        // wait for every MMA / scale copy issued so far before TMEM is freed
+        // wait for this thread's copies before TMEM is freed
+        tc_commit(drain2_bar);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(drain2_bar, 0) && clock64() - t0 < ctl.budget) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================= MMA issuer =============================
+    if (lane == 0 && total_units > 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = decode_unit(u, p, n_tiles, nk);
+        if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
+        const uint32_t idesc = idesc_nvf4(un.nmma);
+        for (int ks = 0; ks < nk; ++ks) {
+          // operands landed (full) and their scales are in tensor memory (scales ready)
+          if (!wait_phase(full_bar(stage), phase, ctl) || !wait_phase(sfr_bar(stage), phase, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int natoms = min(4, kc4 - 4 * ks);
+          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+          const uint32_t sWs = sW + stage * kWStageBytes;
+          for (int a = 0; a < natoms; ++a) {
+            const uint64_t adesc = desc_sw128(sWs + 32 * a);
+            const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        // wait for every MMA issued so far before TMEM is freed
         tc_commit(drain_bar);
         const long long t0 = clock64();
         while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < ctl.budget) {
@@ -439,48 +462,80 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else {
     // ============================== epilogue ==============================
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int quad = warp & 3;     // TMEM lanes 32*quad .. 32*quad+31 = tile rows
+    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    const int half = p.N / 2;
     int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < total_items; it += gridDim.x) {
-      const int u = it / per_unit;
-      const int seg0 = it - u * per_unit, seg1 = p.split ? seg0 + 1 : nseg;
+    uint32_t acc_phase = 0, xph = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
       const Unit un = decode_unit(u, p, n_tiles, nk);
-      const int n = un.nt * kBM + quad * 32 + lane;
-      float sum[kTokChunk];
-      for (int sg = seg0; sg < seg1; ++sg) {
-        if (!wait_phase(accf_bar(acc), acc_phase, ctl)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
-        uint32_t r[kTokChunk];
-        // one load of 16 or 32 columns from the buffer's first column (aligned)
-        if (un.nvalid <= 16) {
-          tc_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
-        } else {
-          tc_ld_32x32b_x32(taddr, r);
-        }
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(acce_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-        if (p.split) {
-          float* dst = p.d + (size_t)sg * p.part_stride + (size_t)un.row0 * p.N + n;
-#pragma unroll
-          for (int j = 0; j < kTokChunk; ++j)
-            if (j < un.nvalid) dst[(size_t)j * p.N] = __uint_as_float(r[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kTokChunk; ++j) sum[j] = sg == 0 ? __uint_as_float(r[j]) : sum[j] + __uint_as_float(r[j]);
-          if (sg == nseg - 1) {
-            float* dst = p.d + (size_t)un.row0 * p.N + n;
-#pragma unroll
-            for (int j = 0; j < kTokChunk; ++j)
-              if (j < un.nvalid) dst[(size_t)j * p.N] = sum[j];
-          }
-        }
+      if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
+      uint32_t r[kTokChunk];
+      // one load of 16 or 32 columns from the buffer's first column (aligned)
+      if (un.nvalid <= 16) {
+        tc_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+      } else {
+        tc_ld_32x32b_x32(taddr, r);
       }
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(acce_bar(acc));  // the accumulator buffer is free again
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      const int tr = quad * 32 + lane;  // tile row
+      if (!p.fused) {
+        const int n = !p.interleaved ? un.nt * kBM + tr
+                                     : (tr < 64 ? un.nt * 64 + tr : half + un.nt * 64 + (tr - 64));
+        float* dst = p.d + (size_t)un.row0 * p.N + n;
+#pragma unroll
+        for (int j = 0; j < kTokChunk; ++j)
+          if (j < un.nvalid) dst[(size_t)j * p.N] = __uint_as_float(r[j]);
+        continue;
+      }
+      // ---- fused SwiGLU + requantize: up rows (lanes 64..127) to smem, gate rows compute ----
+      uint8_t* sfblk = p.h_sf + ((size_t)un.chunk * (half / 64) + un.nt) * kAtomBytes;  // atom nt of the chunk
+      if (quad >= 2) {
+        if (!wait_phase(xfree_bar, xph ^ 1u, ctl)) break;
+        const int f = tr - 64;
+#pragma unroll
+        for (int j = 0; j < kTokChunk; ++j)
+          if (j < un.nvalid) xch[f * kXchStride + j] = __uint_as_float(r[j]);
+        mbar_arrive(xfull_bar);
+      } else {
+        if (!wait_phase(xfull_bar, xph, ctl)) break;
+        const float gg = __ldg(p.g_gate_up + 2 * un.expert), gu = __ldg(p.g_gate_up + 2 * un.expert + 1);
+        uint8_t* hp = p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 + quad * 16 + (lane >> 1);
+#pragma unroll
+        for (int j = 0; j < kTokChunk; ++j) {
+          if (j >= un.nvalid) break;  // uniform across the warp
+          const float gt = __uint_as_float(r[j]) * gg;
+          const float uv = xch[tr * kXchStride + j] * gu;
+          const float hv = gt / (1.0f + expf(-gt)) * uv;
+          const float v = bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));  // h rounded once to bf16
+          float amax = fabsf(v);  // 16-feature block = 16 lanes
+          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
+          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
+          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
+          const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
+          const float dsc = e4m3_decode(sc);
+          const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
+          uint32_t w = code << (4 * (lane & 7));  // 8 features -> one 32-bit word, feature 2i low nibble
+          w |= __shfl_xor_sync(~0u, w, 1);
+          w |= __shfl_xor_sync(~0u, w, 2);
+          w |= __shfl_xor_sync(~0u, w, 4);
+          const uint32_t sc_hi = __shfl_sync(~0u, sc, 16);
+          if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(hp + (size_t)j * (half / 2)) = w;
+          if (lane == 0) *reinterpret_cast<uint16_t*>(sfblk + j * 16 + 2 * quad) = (uint16_t)(sc | (sc_hi << 8));
+        }
+        mbar_arrive(xfree_bar);
+      }
+      xph ^= 1u;
+      // the rest of the chunk's 512-byte scale block (other words, rows past the chunk) is zero
+      const int row = et >> 2, wi = et & 3;
+      if (wi != 0 || row >= un.nvalid) reinterpret_cast<uint32_t*>(sfblk)[et] = 0u;
     }
   }
   __syncwarp();
@@ -521,37 +576,36 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
 
 }  // namespace
 
-int gemm_segments(int K) { return ((K + 255) / 256 + kSegStages - 1) / kSegStages; }
-
 cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
-                                const uint8_t* w_tiled, int E, int N, int K, float* d, size_t part_stride,
-                                bool early, int* status, cudaStream_t s) {
+                                const uint8_t* w_tiled, bool w_interleaved, int E, int N, int K, float* d,
+                                const SwigluOut* swiglu, bool early, int* status, cudaStream_t s) {
   CUtensorMap tmB;
   if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
-  GemmArgs p;
+  GemmArgs p = {};
   p.a_sf = a_sf;
   p.w_tiled = w_tiled;
   p.d = d;
+  if (swiglu) {
+    p.h_packed = swiglu->packed;
+    p.h_sf = swiglu->sf;
+    p.g_gate_up = swiglu->g_gate_up;
+  }
   p.counts = g.counts;
-  p.group_offsets = g.group_offsets;
-  p.group_expert = g.group_expert;
-  p.group_sf_block = g.group_sf_block;
   p.group_chunk = g.group_chunk;
   p.chunk_info = g.chunk_info;
   p.status = status;
   p.N = N;
   p.K = K;
-  p.split = part_stride > 0 ? 1 : 0;
+  p.interleaved = w_interleaved ? 1 : 0;
+  p.fused = swiglu ? 1 : 0;
   p.early = early ? 1 : 0;
-  p.part_stride = part_stride;
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  const long long chunks_bound = (long long)(E < R_max ? E : R_max) + (R_max + kTokChunk - 1) / kTokChunk;
-  const long long units_bound = chunks_bound * (N / kBM) * (part_stride > 0 ? gemm_segments(K) : 1);
+  const long long units_bound = chunks_bound(R_max, E) * (N / kBM);
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
   return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, tmB, p);

@@ -52,16 +52,19 @@ def test_host_side_validation(native):
     g = _fake_groups()
     s = None
     # unsupported GEMM shapes
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 4, 100, 256, 16, s) == 2
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 4, 128, 96, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 0, 4, 100, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 0, 4, 128, 96, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 1, 4, 384, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm_swiglu(16, 16, ctypes.byref(g), 8, 16, 4, 192, 256, 16, 16, 16, s) == 2
     # missing group arrays / bad sizes / misaligned weights
-    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 4, 128, 256, 16, s) == 1
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 24, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 24, 0, 4, 128, 256, 16, s) == 1
     assert native.nvfp4_quantize_rows(16, 8, 100, 4, ctypes.byref(g), 1, 16, 16, s) == 2
     assert native.nvfp4_quantize_rows(16, 8, 128, 0, ctypes.byref(g), 1, 16, 16, s) == 1
     assert native.nvfp4_quantize_rows(16, 8, 128, 4, ctypes.byref(g), 7, 16, 16, s) == 1
-    assert native.nvfp4_tile_weights(16, 16, 100, 128, 16, s) == 2
-    assert native.nvfp4_tile_weights(16, 16, 128, 96, 16, s) == 2
+    assert native.nvfp4_tile_weights(16, 16, 100, 128, 0, 16, s) == 2
+    assert native.nvfp4_tile_weights(16, 16, 128, 96, 0, 16, s) == 2
+    assert native.nvfp4_tile_weights(16, 16, 384, 128, 384, 16, s) == 2
     assert native.moe_route_groups(16, 2, 2, 2000, ctypes.byref(g), s) == 1
     assert native.moe_route_groups(16, 2, 40, 8, ctypes.byref(g), s) == 1
     assert native.moe_scatter_add(16, 256, 16, 16, 2, 2, -1, ctypes.byref(g), 16, 16, s) == 1

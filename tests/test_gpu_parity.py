@@ -126,11 +126,20 @@ def test_swizzle_matches_oracle(cuda):
         assert np.array_equal(out.cpu().numpy(), O.swizzle_scales(lin))
 
 
-def expected_tiled(packed: np.ndarray, sf_linear: np.ndarray, K: int) -> np.ndarray:
+def expected_tiled(packed: np.ndarray, sf_linear: np.ndarray, K: int, interleave: int = 0) -> np.ndarray:
     """The GEMM tiling built independently on the host: per 128-row tile and
     256-value stage, rows' 16-byte chunks at chunk c ^ (r % 8), then the
-    stage's scale atoms (the oracle's atom layout)."""
+    stage's scale atoms (the oracle's atom layout). interleave = n > 0 first
+    reorders every n rows so that tile t holds rows 64t..64t+63 of the first
+    half and the same rows of the second half."""
     rows = packed.shape[0]
+    if interleave:
+        src = []
+        for b in range(rows // interleave):
+            for t in range(interleave // 128):
+                src += [b * interleave + 64 * t + j for j in range(64)]
+                src += [b * interleave + interleave // 2 + 64 * t + j for j in range(64)]
+        packed, sf_linear = packed[src], sf_linear[src]
     nk, kc4, rowb = (K + 255) // 256, K // 64, K // 2
     pad = np.zeros((rows, nk * 128), np.uint8)
     pad[:, :rowb] = packed
@@ -151,13 +160,15 @@ def expected_tiled(packed: np.ndarray, sf_linear: np.ndarray, K: int) -> np.ndar
     return out.reshape(-1)
 
 
-@pytest.mark.parametrize("rows,K", [(256, 256), (128, 384), (384, 128)])
-def test_tile_weights_layout(cuda, rows, K):
-    rng = np.random.default_rng(rows + K)
-    packed = rng.integers(0, 256, (1, rows, K // 2), dtype=np.uint8)
-    sfl = rng.integers(0, 256, (1, rows, K // 16), dtype=np.uint8)
-    tw = N.TiledWeight(torch.from_numpy(packed).to(cuda), torch.from_numpy(sfl).to(cuda))
-    assert np.array_equal(tw.data.cpu().numpy(), expected_tiled(packed[0], sfl[0], K))
+@pytest.mark.parametrize("E,rows,K,il", [(1, 256, 256, False), (1, 128, 384, False), (1, 384, 128, False),
+                                         (2, 256, 256, True), (3, 512, 192, True)])
+def test_tile_weights_layout(cuda, E, rows, K, il):
+    rng = np.random.default_rng(rows + K + E)
+    packed = rng.integers(0, 256, (E, rows, K // 2), dtype=np.uint8)
+    sfl = rng.integers(0, 256, (E, rows, K // 16), dtype=np.uint8)
+    tw = N.TiledWeight(torch.from_numpy(packed).to(cuda), torch.from_numpy(sfl).to(cuda), interleave=il)
+    want = expected_tiled(packed.reshape(E * rows, -1), sfl.reshape(E * rows, -1), K, rows if il else 0)
+    assert np.array_equal(tw.data.cpu().numpy(), want)
 
 
 # ---------------------------------------------------------------------------
@@ -304,6 +315,13 @@ def test_swiglu_requant_fused_equals_separate(small):
     N.swiglu_quantize_grouped(st["d13"], G, W.g_gate_up, p, s)
     R = st["groups"]["R"]
     assert torch.equal(p[:R], st["hq"][:R]) and torch.equal(s, st["hsf"])
+    # the w13 GEMM with SwiGLU + requantization in its epilogue equals the
+    # separate GEMM, SwiGLU and quantize kernels, nibbles and scales
+    for _ in range(3):
+        p2 = torch.zeros_like(st["hq"])
+        s2 = torch.zeros_like(st["hsf"])
+        N.nvfp4_grouped_gemm_swiglu(st["xq"], st["xsf"], G, W.w13, W.g_gate_up, p2, s2)
+        assert torch.equal(p2[:R], st["hq"][:R]) and torch.equal(s2, st["hsf"])
 
 
 def test_layer_determinism_and_batch_invariance(small):
