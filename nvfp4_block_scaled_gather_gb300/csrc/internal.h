@@ -35,8 +35,9 @@ inline size_t token_sf_bytes(long long R_max, long long G_max, long long K, int 
 
 int num_sms();  // SM count of the current device (cached per device)
 
-cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g,
-                         cudaStream_t s);
+// zero/nzero: an int array the route kernel also clears (may be null).
+cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s,
+                         int* zero = nullptr, int nzero = 0);
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g,
                           uint16_t* xg, cudaStream_t s);
 // src_k > 0: rows are x[row_slot[r] / src_k]; src_k == 0: rows are src[r].
@@ -56,24 +57,39 @@ cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, cons
                            int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s);
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s);
 
-// tcgen05 grouped GEMM (nvfp4_gemm.cu). status: device word for wait timeouts.
+// tcgen05 grouped GEMM (nvfp4_gemm.cu), one persistent launch over one or
+// two jobs. A job: token rows a_packed [R_max, K/2] with token scales a_sf
+// (MOE_SF_CHUNK32), tiled weights [E, N, K], fp32 output d [R_max, N].
 // w_interleaved: each 128-row weight tile holds 64 rows of the first half of
 // N and the matching 64 rows of the second half (nvfp4_tile_weights with
-// interleave). swiglu == nullptr: d gets fp32 rows in natural column order.
-// swiglu != nullptr (needs w_interleaved, N = 2I): the epilogue applies
-// SwiGLU with the per-expert (gate, up) globals and writes NVFP4 h (packed
-// [R_max, I/2], token scales MOE_SF_CHUNK32), bit-identical to swiglu_grouped
-// followed by nvfp4_quantize_rows; d is not written.
-// early: the group metadata and the weights were written two or more
+// interleave); d still gets natural column order.
+// swiglu != nullptr (job 0 needs w_interleaved, N = 2I): job 0's epilogue
+// applies SwiGLU with the per-expert (gate, up) globals and writes NVFP4 h
+// (packed [R_max, I/2], token scales MOE_SF_CHUNK32), bit-identical to
+// swiglu_grouped followed by nvfp4_quantize_rows; job 0's d is not written.
+// j1 != nullptr: job 1 runs in the same launch and may read what job 0
+// wrote: a job-1 unit of a 32-row chunk starts its token loads once all of
+// job 0's tiles of that chunk are done. gate holds 1 + chunks_bound(R_max, E)
+// ints, zero at launch: the unit claim counter, then the per-chunk counts of
+// finished job-0 tiles.
+// early: the group metadata, gate and the weights were written two or more
 // launches back (true inside moe_nvfp4_layer), so the GEMM may read them and
 // start streaming weights before the previous kernel has finished.
+// status: device word that records a wait timeout (MOE_ERR_TIMEOUT).
 struct SwigluOut {
   uint8_t* packed;
   uint8_t* sf;
   const float* g_gate_up;
 };
-cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
-                                const uint8_t* w_tiled, bool w_interleaved, int E, int N, int K, float* d,
-                                const SwigluOut* swiglu, bool early, int* status, cudaStream_t s);
+struct GemmJob {
+  const uint8_t* a_packed;
+  const uint8_t* a_sf;
+  const uint8_t* w_tiled;
+  bool w_interleaved;
+  int N, K;
+  float* d;
+};
+cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
+                                const GemmJob* j1, int* gate, bool early, int* status, cudaStream_t s);
 
 }  // namespace moe

@@ -55,6 +55,8 @@ struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
   float* d2;
+  int* gate;  // the GEMM's unit claim counter, then w13 tiles finished per 32-row chunk
+  int ngate;
   size_t bytes;
 };
 
@@ -75,6 +77,8 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   w.hq = take(S * I / 2);
   w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
   w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
+  w.ngate = 1 + (int)chunks_bound((long long)S, E);
+  w.gate = reinterpret_cast<int*>(take((size_t)w.ngate * sizeof(int)));
   w.bytes = off;
   return w;
 }
@@ -200,8 +204,8 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
     return MOE_ERR_INVALID;
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
-  return status_of(launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w_tiled, w_interleaved != 0, E, N, K, d,
-                                       nullptr, false, st, stream));
+  const GemmJob job{a_packed, a_sf, w_tiled, w_interleaved != 0, N, K, d};
+  return status_of(launch_grouped_gemm(*groups, R_max, E, job, nullptr, nullptr, nullptr, false, st, stream));
 }
 
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
@@ -219,8 +223,8 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
   const SwigluOut out{h_packed, h_sf, g_gate_up};
-  return status_of(
-      launch_grouped_gemm(a_packed, a_sf, *groups, R_max, w13_tiled, true, E, 2 * I, K, nullptr, &out, false, st, stream));
+  const GemmJob job{a_packed, a_sf, w13_tiled, true, 2 * I, K, nullptr};
+  return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, false, st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -277,15 +281,15 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
   const int S = T * k;
-  cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
+  cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate);
   if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
-  const SwigluOut swiglu{ws.hq, ws.hsf, w->g_gate_up};  // a5 + a6 in the w13 GEMM's epilogue
+  // a4 + a5 + a6 (w13 with SwiGLU and requantization in its epilogue) and a7
+  // (w2) in one persistent launch; a w2 unit starts once its chunk's h is in
+  const SwigluOut swiglu{ws.hq, ws.hsf, w->g_gate_up};
+  const GemmJob w13{ws.xq, ws.xsf, w->w13_tiled, true, 2 * I, H, nullptr};
+  const GemmJob w2{ws.hq, ws.hsf, w->w2_tiled, false, H, I, ws.d2};
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.xq, ws.xsf, ws.groups, S, w->w13_tiled, true, E, 2 * I, H, nullptr, &swiglu, true,
-                              st, stream);
-  if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.hq, ws.hsf, ws.groups, S, w->w2_tiled, false, E, H, I, ws.d2, nullptr, true, st,
-                              stream);
+    err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, true, st, stream);
   if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
 }

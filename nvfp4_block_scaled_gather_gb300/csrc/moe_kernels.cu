@@ -41,9 +41,10 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
 // Rows therefore ascend by (expert, slot), a pure function of the routing.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__ ids, int S, int E,
-                                                     moe_groups_t g) {
+                                                     moe_groups_t g, int* __restrict__ zero, int nzero) {
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
+  for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   extern __shared__ int32_t smem[];
   int32_t* wc = smem;                // [32][E]: counts, then running row cursors
   int32_t* rowbase = smem + 32 * E;  // [E]: first row of each expert
@@ -475,13 +476,14 @@ int grid_for(long long items) {
 
 }  // namespace
 
-cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s) {
+cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s, int* zero,
+                         int nzero) {
   const size_t smem = (size_t)33 * E * sizeof(int32_t);
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  return launch_pdl(route_kernel, dim3(1), dim3(1024), smem, s, topk_ids, S, E, g);
+  return launch_pdl(route_kernel, dim3(1), dim3(1024), smem, s, topk_ids, S, E, g, zero, zero ? nzero : 0);
 }
 
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g, uint16_t* xg,

@@ -66,21 +66,32 @@ constexpr int kSmemBytes = 114688;  // per CTA: two CTAs fit the SM's 228 KB (1 
 constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
 constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: up values [64][33] floats
 constexpr int kXchBytes = 9216;                    // 64 * 33 * 4 rounded up to 1 KB
+constexpr int kUq = 8;                             // unit queue: producer -> MMA, scale copies, epilogue
+constexpr int kUqReaders = 1 + 1 + 128;
+
+// One grouped GEMM over the routed rows: weights (tiled), token operand
+// (TMA map passed beside the arguments), token scales, output.
+struct Job {
+  const uint8_t* w_tiled;
+  const uint8_t* a_sf;      // token scales, MOE_SF_CHUNK32, K wide
+  float* d;                 // plain epilogue: fp32 rows [R_max, N]
+  int N, K;
+  int interleaved;          // tiles hold 64 rows of each half of N
+};
 
 struct GemmArgs {
-  const uint8_t* a_sf;
-  const uint8_t* w_tiled;
-  float* d;                 // plain epilogue: fp32 rows [R_max, N]
-  uint8_t* h_packed;        // fused epilogue: NVFP4 h [R_max, N/2 / 2] ...
-  uint8_t* h_sf;            // ... and its token scales (MOE_SF_CHUNK32, K = N/2)
+  Job j0, j1;               // j1 is used when njobs == 2
+  int njobs;
+  int fused0;               // job 0: SwiGLU + requantize epilogue (needs interleaved)
+  uint8_t* h_packed;        // ... NVFP4 h [R_max, N0/4] ...
+  uint8_t* h_sf;            // ... and its token scales (MOE_SF_CHUNK32, K = N0/2) ...
   const float* g_gate_up;   // ... with the per-expert (gate, up) globals
+  int* chunk_done;          // njobs == 2: job-0 tiles finished per chunk (zero at launch)
+  int* work_ctr;            // njobs == 2: next unit to claim (zero at launch)
   const int32_t* counts;
   const int32_t* group_chunk;
   const int32_t* chunk_info;
   int* status;
-  int N, K;
-  int interleaved;          // tiles hold 64 gate rows then 64 up rows (halves of N)
-  int fused;                // 1: SwiGLU + requantize epilogue (needs interleaved)
   int early;                // 1: group metadata and weights were written two or more launches back
   long long wait_budget;    // clock64 cycles a single wait may take
 };
@@ -172,6 +183,19 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[3
       : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's view of global memory (after an acquire) before its
+// later async-proxy (TMA, bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // that TMA writes: rows of 128 bytes, 8-row groups 1024 bytes apart
@@ -197,6 +221,11 @@ struct Ctl {
   long long budget;
 };
 
+__device__ __forceinline__ void give_up(const Ctl& c) {
+  *c.abort_flag = 1;
+  atomicExch(c.status, (int)MOE_ERR_TIMEOUT);
+}
+
 // Bounded wait: false if this or another role gave up.
 __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -205,43 +234,64 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl
     if (mbar_try_wait(bar, parity)) return true;
     if (*c.abort_flag) return false;
     if (clock64() - t0 > c.budget) {
-      *c.abort_flag = 1;
-      atomicExch(c.status, (int)MOE_ERR_TIMEOUT);
+      give_up(c);
       return false;
     }
   }
 }
 
-// One unit of work: 32-row chunk `chunk` of a group (its rows [32q, 32q+32))
-// against 128-row weight tile `nt` of the group's expert. The chunk's token
-// scales are one 512-byte block per K-atom (layout MOE_SF_CHUNK32), copied to
-// TMEM with tcgen05.cp.32x128b.warpx4 at a 4-column-aligned address.
+// Bounded wait until another CTA's counter reaches target (acquire), then a
+// proxy fence so that this thread's TMA reads see what those CTAs wrote.
+__device__ __noinline__ bool wait_count(const int* ctr, int target, const Ctl& c) {
+  const long long t0 = clock64();
+  while (ld_acquire(ctr) < target) {
+    if (*c.abort_flag) return false;
+    if (clock64() - t0 > c.budget) {
+      give_up(c);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// One unit of work: 32-row chunk `chunk` of a group against 128-row weight
+// tile `nt` of the group's expert, for job 0 (units [0, U0)) or job 1. The
+// chunk's token scales are one 512-byte block per K-atom (MOE_SF_CHUNK32).
 struct Unit {
-  int chunk, row0, nvalid, nmma, nt, expert;
-  size_t w_off, sfb_off;
+  int job, chunk, row0, nvalid, nmma, nt, expert, nk, kc4;
+  const uint8_t* w;    // the tile's first 18 KB stage
+  const uint8_t* sfb;  // the chunk's first token-scale block
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int n_tiles, int nk) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int U0, int nt0, int nt1) {
   Unit un;
-  un.chunk = u / n_tiles;
-  un.nt = u - un.chunk * n_tiles;
+  un.job = u >= U0 ? 1 : 0;
+  const int v = un.job ? u - U0 : u;
+  const int ntl = un.job ? nt1 : nt0;
+  un.chunk = v / ntl;
+  un.nt = v - un.chunk * ntl;
   const int4 c = __ldg(reinterpret_cast<const int4*>(p.chunk_info) + un.chunk);  // row0, rows, expert, group
   un.row0 = c.x;
   un.nvalid = c.y;
   un.expert = c.z;
   un.nmma = (un.nvalid + 15) & ~15;
-  un.w_off = ((size_t)un.expert * n_tiles + un.nt) * nk * kWStageBytes;
-  un.sfb_off = (size_t)un.chunk * (p.K / 64) * kAtomBytes;
+  const int K = un.job ? p.j1.K : p.j0.K;
+  un.nk = (K + 255) / 256;
+  un.kc4 = K / 64;
+  un.w = (un.job ? p.j1.w_tiled : p.j0.w_tiled) + ((size_t)un.expert * ntl + un.nt) * un.nk * kWStageBytes;
+  un.sfb = (un.job ? p.j1.a_sf : p.j0.a_sf) + (size_t)un.chunk * un.kc4 * kAtomBytes;
   return un;
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain, scales_ready[16], drain2,
-  // xch_full, xch_free
+  // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain, scales_ready[16], unit_done,
+  // xch_full, xch_free, drain2
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -249,11 +299,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
   auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * kMaxStages + 5 + s); };
-  const uint32_t drain2_bar = bar0 + 8u * (3 * kMaxStages + 5);
+  const uint32_t udone_bar = bar0 + 8u * (3 * kMaxStages + 5);
   const uint32_t xfull_bar = bar0 + 8u * (3 * kMaxStages + 6);
   const uint32_t xfree_bar = bar0 + 8u * (3 * kMaxStages + 7);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 516);
+  const uint32_t drain2_bar = bar0 + 8u * (3 * kMaxStages + 8);
+  auto uqf_bar = [&](int i) { return bar0 + 8u * (3 * kMaxStages + 9 + i); };
+  auto uqe_bar = [&](int i) { return bar0 + 8u * (3 * kMaxStages + 9 + kUq + i); };
+  // after the barriers (< 640 bytes): TMEM address, abort flag, unit queue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 640);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 644);
+  volatile int* uq = reinterpret_cast<volatile int*>(smem + 704);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Programmatic dependent launch: this grid may start while the previous
@@ -269,14 +324,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int G = __ldg(p.counts + 0);
   const int maxmg = __ldg(p.counts + 2);
   const int nchunks = G > 0 ? __ldg(p.group_chunk + G) : 0;
-  const int n_tiles = p.N / kBM;
-  const int total_units = nchunks * n_tiles;
-  const int kc4 = p.K / 64;               // scale atoms along K per row block
-  const int nk = (p.K + 255) / 256;       // stages per unit
+  const int nt0 = p.j0.N / kBM;
+  const int nt1 = p.njobs > 1 ? p.j1.N / kBM : 1;
+  const int U0 = nchunks * nt0;
+  const int total_units = U0 + (p.njobs > 1 ? nchunks * nt1 : 0);
+  const bool has_xch = p.fused0 != 0;
   const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
   const int acc_cols = max(32, tn);
   const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
-  const int avail = kSmemBytes - 1024 - 1024 - (p.fused ? kXchBytes : 0);
+  const int avail = kSmemBytes - 1024 - 1024 - (has_xch ? kXchBytes : 0);
   int stages = min(kMaxStages, avail / stage_bytes);
   stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
   // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, token scales, exchange
@@ -297,8 +353,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     mbar_init(drain_bar, 1);
     mbar_init(drain2_bar, 1);
+    mbar_init(udone_bar, 4 * 32);
     mbar_init(xfull_bar, 64);
     mbar_init(xfree_bar, 64);
+    for (int i = 0; i < kUq; ++i) {
+      mbar_init(uqf_bar(i), 1);
+      mbar_init(uqe_bar(i), kUqReaders);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -314,67 +375,144 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.wait_budget};
+  // The producer hands every role the same unit sequence through the queue:
+  // unit ids, then -1. Returns the next unit, -1 at the end, -2 on a timeout.
+  int q_idx = 0;
+  uint32_t q_phase = 0;
+  auto next_unit = [&]() -> int {
+    if (!wait_phase(uqf_bar(q_idx), q_phase, ctl)) return -2;
+    const int u = uq[q_idx];
+    mbar_arrive(uqe_bar(q_idx));
+    if (++q_idx == kUq) { q_idx = 0; q_phase ^= 1u; }
+    return u;
+  };
 
   if (warp == 0) {
     // ============================ TMA producer ============================
-    if (lane == 0 && total_units == 0 && p.early) {
-      pdl_wait();
-      pdl_trigger();
-    }
-    if (lane == 0 && total_units > 0) {
+    // Units are taken in increasing order: with two jobs from a global
+    // counter (every job-0 unit is claimed, by a running CTA, before any
+    // job-1 unit, so a job-1 wait always ends however many CTAs are
+    // resident), otherwise blockIdx.x, blockIdx.x + gridDim.x, ...
+    if (lane == 0) {
+      const bool dynamic = p.work_ctr != nullptr;
+      int static_next = blockIdx.x;
+      auto claim = [&]() -> int {
+        int u;
+        if (dynamic) {
+          u = atomicAdd(p.work_ctr, 1);
+        } else {
+          u = static_next;
+          static_next += gridDim.x;
+        }
+        return u < total_units ? u : -1;
+      };
+      int wq = 0;
+      uint32_t wq_phase = 0;
+      bool ok = true;
+      auto push = [&](int u) {
+        if (!wait_phase(uqe_bar(wq), wq_phase ^ 1u, ctl)) return false;
+        uq[wq] = u;
+        mbar_arrive(uqf_bar(wq));
+        if (++wq == kUq) { wq = 0; wq_phase ^= 1u; }
+        return true;
+      };
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
-      bool ok = true;
       const uint64_t stream_policy = policy_evict_first();
-      // With p.early, the weight copies of the first ring slots go out before
+      // With p.early, the first unit's first weight stages go out before
       // waiting for the previous kernel (they do not depend on it); the token
       // rows and their scales follow once it has completed.
+      int cur = (total_units > 0) ? claim() : -1;
       int prefetched = 0;
       if (p.early) {
-        int u = blockIdx.x, ks = 0;
-        Unit un = decode_unit(u < total_units ? u : 0, p, n_tiles, nk);
-        for (int slot = 0; slot < stages && u < total_units; ++slot) {
-          const int natoms = min(4, kc4 - 4 * ks);
-          const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
-          mbar_expect_tx_only(full_bar(slot), wbytes);
-          bulk_load_hint(sW + slot * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes,
-                         full_bar(slot), stream_policy);
-          ++prefetched;
-          if (++ks == nk) {
-            ks = 0;
-            u += gridDim.x;
-            if (u < total_units) un = decode_unit(u, p, n_tiles, nk);
+        if (cur >= 0) {
+          const Unit un = decode_unit(cur, p, U0, nt0, nt1);
+          for (int ks = 0; ks < un.nk && ks < stages; ++ks) {
+            const int natoms = min(4, un.kc4 - 4 * ks);
+            const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
+            mbar_expect_tx_only(full_bar(ks), wbytes);
+            bulk_load_hint(sW + ks * kWStageBytes, un.w + (size_t)ks * kWStageBytes, wbytes, full_bar(ks),
+                           stream_policy);
+            ++prefetched;
           }
         }
         pdl_wait();
         pdl_trigger();
       }
       int issued = 0;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit un = decode_unit(u, p, n_tiles, nk);
+      while (ok) {
+        if (!push(cur)) { ok = false; break; }
+        if (cur < 0) break;
+        const Unit un = decode_unit(cur, p, U0, nt0, nt1);
+        const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
         const int nbox = un.nmma / kBBoxRows;
-        for (int ks = 0; ks < nk; ++ks, ++issued) {
-          const int natoms = min(4, kc4 - 4 * ks);
+        // token rows + scales of stage ks into ring slot `slot` (pre: its
+        // weights were prefetched, so this is the stage's arrival)
+        auto issue_tokens = [&](int slot, int ks, bool pre) {
+          const int natoms = min(4, un.kc4 - 4 * ks);
+          const uint32_t fb = full_bar(slot);
+          if (pre) mbar_expect_tx(fb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(sB + slot * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, map, ks * kStageKBytes,
+                        un.row0 + b * kBBoxRows, fb);
+          bulk_load(sSFB + slot * kSfStageBytes, un.sfb + (size_t)ks * kSfStageBytes, natoms * kAtomBytes, fb);
+        };
+        // Job 1 reads h, which job 0 writes: its weights stream at once, its
+        // token copies wait until every job-0 tile of the chunk is done
+        // (pending stages, at most a ring's worth).
+        bool dep = un.job == 0;
+        int pend_n = 0, pend_ks = 0, pend_slot = 0, pend_issued = 0;
+        auto flush = [&]() {
+          for (int j = 0; j < pend_n; ++j) {
+            int slot = pend_slot + j;
+            if (slot >= stages) slot -= stages;
+            issue_tokens(slot, pend_ks + j, pend_issued + j < prefetched);
+          }
+          pend_n = 0;
+        };
+        for (int ks = 0; ks < un.nk; ++ks, ++issued) {
+          if (pend_n == stages) {
+            // every slot waits for h: the next one cannot be refilled before it arrives.
+            // On a timeout the (in-bounds) token copies are still issued so that
+            // the slots' phases complete and the drain below ends.
+            const bool got = wait_count(p.chunk_done + un.chunk, nt0, ctl);
+            flush();
+            dep = true;
+            if (!got) { ok = false; break; }
+          }
+          const int natoms = min(4, un.kc4 - 4 * ks);
           const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
           const uint32_t tbytes = nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
           const uint32_t fb = full_bar(stage);
-          if (issued < prefetched) {
-            mbar_expect_tx(fb, tbytes);  // weights already on their way
-          } else {
+          if (issued >= prefetched) {
             if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
             mbar_expect_tx(fb, wbytes + tbytes);
-            bulk_load_hint(sW + stage * kWStageBytes, p.w_tiled + un.w_off + (size_t)ks * kWStageBytes, wbytes, fb,
-                           stream_policy);
+            bulk_load_hint(sW + stage * kWStageBytes, un.w + (size_t)ks * kWStageBytes, wbytes, fb, stream_policy);
           }
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, &tmB, ks * kStageKBytes,
-                        un.row0 + b * kBBoxRows, fb);
-          bulk_load(sSFB + stage * kSfStageBytes, p.a_sf + un.sfb_off + (size_t)ks * kSfStageBytes,
-                    natoms * kAtomBytes, fb);
           filled |= 1u << stage;
           fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (!dep) {
+            if (pend_n == 0) { pend_ks = ks; pend_slot = stage; pend_issued = issued; }
+            ++pend_n;
+            if (ld_acquire(p.chunk_done + un.chunk) >= nt0) {
+              fence_proxy_async_global();
+              dep = true;
+              flush();
+            }
+          } else {
+            issue_tokens(stage, ks, issued < prefetched);
+          }
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
+        if (pend_n > 0) {
+          const bool got = wait_count(p.chunk_done + un.chunk, nt0, ctl);
+          flush();
+          if (!got) ok = false;
+        }
+        // the next unit is claimed once this one's copies are all issued (a
+        // ring's worth of stages still in flight hides the atomic's latency);
+        // claiming earlier would let a CTA hoard units behind a job-1 wait
+        cur = claim();
       }
       if (!ok) {
         // let every copy this thread issued land before the CTA exits
@@ -388,13 +526,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == 6) {
     // ======================== scale copies into TMEM =======================
-    // Stage slot s's scale columns are rewritten only after the slot was
-    // refilled, i.e. after the MMAs that read them completed (empty[s]).
-    if (lane == 0 && total_units > 0) {
+    // Slot s's scale columns are rewritten only after the slot was refilled,
+    // i.e. after the MMAs that read them completed (empty[s]).
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      while (ok) {
+        const int u = next_unit();
+        if (u < 0) { ok = u == -1; break; }
+        const int K = u >= U0 ? p.j1.K : p.j0.K;
+        const int nk = (K + 255) / 256, kc4 = K / 64;
         for (int ks = 0; ks < nk; ++ks) {
           if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
           tc_fence_after();
@@ -419,24 +561,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == 1) {
     // ============================= MMA issuer =============================
-    if (lane == 0 && total_units > 0) {
+    if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit un = decode_unit(u, p, n_tiles, nk);
+      while (ok) {
+        const int u = next_unit();
+        if (u < 0) { ok = u == -1; break; }
+        const Unit un = decode_unit(u, p, U0, nt0, nt1);
         if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
         const uint32_t idesc = idesc_nvf4(un.nmma);
-        for (int ks = 0; ks < nk; ++ks) {
+        for (int ks = 0; ks < un.nk; ++ks) {
           // operands landed (full) and their scales are in tensor memory (scales ready)
           if (!wait_phase(full_bar(stage), phase, ctl) || !wait_phase(sfr_bar(stage), phase, ctl)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int natoms = min(4, kc4 - 4 * ks);
+          const int natoms = min(4, un.kc4 - 4 * ks);
           const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
           const uint32_t sWs = sW + stage * kWStageBytes;
           for (int a = 0; a < natoms; ++a) {
@@ -464,11 +608,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ============================== epilogue ==============================
     const int quad = warp & 3;     // TMEM lanes 32*quad .. 32*quad+31 = tile rows
     const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
-    const int half = p.N / 2;
+    const int half = p.j0.N / 2;
     int acc = 0;
-    uint32_t acc_phase = 0, xph = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const Unit un = decode_unit(u, p, n_tiles, nk);
+    uint32_t acc_phase = 0, xph = 0, uph = 0;
+    while (true) {
+      const int u = next_unit();
+      if (u < 0) break;
+      const Unit un = decode_unit(u, p, U0, nt0, nt1);
       if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
@@ -485,57 +631,69 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
       const int tr = quad * 32 + lane;  // tile row
-      if (!p.fused) {
-        const int n = !p.interleaved ? un.nt * kBM + tr
-                                     : (tr < 64 ? un.nt * 64 + tr : half + un.nt * 64 + (tr - 64));
-        float* dst = p.d + (size_t)un.row0 * p.N + n;
+      if (un.job == 1 || !p.fused0) {
+        const int N = un.job ? p.j1.N : p.j0.N;
+        const int il = un.job ? p.j1.interleaved : p.j0.interleaved;
+        const int n = !il ? un.nt * kBM + tr : (tr < 64 ? un.nt * 64 + tr : N / 2 + un.nt * 64 + (tr - 64));
+        float* dst = (un.job ? p.j1.d : p.j0.d) + (size_t)un.row0 * N + n;
 #pragma unroll
         for (int j = 0; j < kTokChunk; ++j)
-          if (j < un.nvalid) dst[(size_t)j * p.N] = __uint_as_float(r[j]);
-        continue;
-      }
-      // ---- fused SwiGLU + requantize: up rows (lanes 64..127) to smem, gate rows compute ----
-      uint8_t* sfblk = p.h_sf + ((size_t)un.chunk * (half / 64) + un.nt) * kAtomBytes;  // atom nt of the chunk
-      if (quad >= 2) {
-        if (!wait_phase(xfree_bar, xph ^ 1u, ctl)) break;
-        const int f = tr - 64;
-#pragma unroll
-        for (int j = 0; j < kTokChunk; ++j)
-          if (j < un.nvalid) xch[f * kXchStride + j] = __uint_as_float(r[j]);
-        mbar_arrive(xfull_bar);
+          if (j < un.nvalid) dst[(size_t)j * N] = __uint_as_float(r[j]);
       } else {
-        if (!wait_phase(xfull_bar, xph, ctl)) break;
-        const float gg = __ldg(p.g_gate_up + 2 * un.expert), gu = __ldg(p.g_gate_up + 2 * un.expert + 1);
-        uint8_t* hp = p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 + quad * 16 + (lane >> 1);
+        // ---- fused SwiGLU + requantize: up rows (lanes 64..127) to smem, gate rows compute ----
+        uint8_t* sfblk = p.h_sf + ((size_t)un.chunk * (half / 64) + un.nt) * kAtomBytes;  // atom nt of the chunk
+        if (quad >= 2) {
+          if (!wait_phase(xfree_bar, xph ^ 1u, ctl)) break;
+          const int f = tr - 64;
 #pragma unroll
-        for (int j = 0; j < kTokChunk; ++j) {
-          if (j >= un.nvalid) break;  // uniform across the warp
-          const float gt = __uint_as_float(r[j]) * gg;
-          const float uv = xch[tr * kXchStride + j] * gu;
-          const float hv = gt / (1.0f + expf(-gt)) * uv;
-          const float v = bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));  // h rounded once to bf16
-          float amax = fabsf(v);  // 16-feature block = 16 lanes
-          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
-          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
-          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
-          amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
-          const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
-          const float dsc = e4m3_decode(sc);
-          const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
-          uint32_t w = code << (4 * (lane & 7));  // 8 features -> one 32-bit word, feature 2i low nibble
-          w |= __shfl_xor_sync(~0u, w, 1);
-          w |= __shfl_xor_sync(~0u, w, 2);
-          w |= __shfl_xor_sync(~0u, w, 4);
-          const uint32_t sc_hi = __shfl_sync(~0u, sc, 16);
-          if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(hp + (size_t)j * (half / 2)) = w;
-          if (lane == 0) *reinterpret_cast<uint16_t*>(sfblk + j * 16 + 2 * quad) = (uint16_t)(sc | (sc_hi << 8));
+          for (int j = 0; j < kTokChunk; ++j)
+            if (j < un.nvalid) xch[f * kXchStride + j] = __uint_as_float(r[j]);
+          mbar_arrive(xfull_bar);
+        } else {
+          if (!wait_phase(xfull_bar, xph, ctl)) break;
+          const float gg = __ldg(p.g_gate_up + 2 * un.expert), gu = __ldg(p.g_gate_up + 2 * un.expert + 1);
+          uint8_t* hp = p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 + quad * 16 + (lane >> 1);
+#pragma unroll
+          for (int j = 0; j < kTokChunk; ++j) {
+            if (j >= un.nvalid) break;  // uniform across the warp
+            const float gt = __uint_as_float(r[j]) * gg;
+            const float uv = xch[tr * kXchStride + j] * gu;
+            const float hv = gt / (1.0f + expf(-gt)) * uv;
+            const float v = bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));  // h rounded once to bf16
+            float amax = fabsf(v);  // 16-feature block = 16 lanes
+            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
+            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
+            const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
+            const float dsc = e4m3_decode(sc);
+            const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
+            uint32_t w = code << (4 * (lane & 7));  // 8 features -> one 32-bit word, feature 2i low nibble
+            w |= __shfl_xor_sync(~0u, w, 1);
+            w |= __shfl_xor_sync(~0u, w, 2);
+            w |= __shfl_xor_sync(~0u, w, 4);
+            const uint32_t sc_hi = __shfl_sync(~0u, sc, 16);
+            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(hp + (size_t)j * (half / 2)) = w;
+            if (lane == 0) *reinterpret_cast<uint16_t*>(sfblk + j * 16 + 2 * quad) = (uint16_t)(sc | (sc_hi << 8));
+          }
+          mbar_arrive(xfree_bar);
         }
-        mbar_arrive(xfree_bar);
+        xph ^= 1u;
+        // the rest of the chunk's 512-byte scale block (other words, rows past the chunk) is zero
+        const int row = et >> 2, wi = et & 3;
+        if (wi != 0 || row >= un.nvalid) reinterpret_cast<uint32_t*>(sfblk)[et] = 0u;
       }
-      xph ^= 1u;
-      // the rest of the chunk's 512-byte scale block (other words, rows past the chunk) is zero
-      const int row = et >> 2, wi = et & 3;
-      if (wi != 0 || row >= un.nvalid) reinterpret_cast<uint32_t*>(sfblk)[et] = 0u;
+      if (un.job == 0 && p.njobs > 1) {
+        // publish this tile of the chunk to job 1: the writers' arrivals
+        // (release, CTA scope) reach one thread, whose release-add at GPU
+        // scope makes all of them visible to the acquiring reader
+        mbar_arrive(udone_bar);
+        if (et == 0) {
+          if (!wait_phase(udone_bar, uph, ctl)) break;
+          red_release_add(p.chunk_done + un.chunk, 1);
+        }
+        uph ^= 1u;
+      }
     }
   }
   __syncwarp();
@@ -576,28 +734,38 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t& g, int R_max,
-                                const uint8_t* w_tiled, bool w_interleaved, int E, int N, int K, float* d,
-                                const SwigluOut* swiglu, bool early, int* status, cudaStream_t s) {
-  CUtensorMap tmB;
-  if (!make_map(&tmB, a_packed, (uint64_t)K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
+cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
+                                const GemmJob* j1, int* gate, bool early, int* status, cudaStream_t s) {
+  CUtensorMap tmB0, tmB1;
+  if (!make_map(&tmB0, j0.a_packed, (uint64_t)j0.K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
+  if (j1 && !make_map(&tmB1, j1->a_packed, (uint64_t)j1->K / 2, (uint64_t)R_max, kBBoxRows))
+    return cudaErrorInvalidValue;
+  if (!j1) tmB1 = tmB0;
+  if (j1 && !gate) return cudaErrorInvalidValue;
   GemmArgs p = {};
-  p.a_sf = a_sf;
-  p.w_tiled = w_tiled;
-  p.d = d;
+  auto fill = [](Job& J, const GemmJob& src) {
+    J.w_tiled = src.w_tiled;
+    J.a_sf = src.a_sf;
+    J.d = src.d;
+    J.N = src.N;
+    J.K = src.K;
+    J.interleaved = src.w_interleaved ? 1 : 0;
+  };
+  fill(p.j0, j0);
+  if (j1) fill(p.j1, *j1);
+  p.njobs = j1 ? 2 : 1;
+  p.fused0 = swiglu ? 1 : 0;
   if (swiglu) {
     p.h_packed = swiglu->packed;
     p.h_sf = swiglu->sf;
     p.g_gate_up = swiglu->g_gate_up;
   }
+  p.work_ctr = j1 ? gate : nullptr;
+  p.chunk_done = j1 ? gate + 1 : nullptr;
   p.counts = g.counts;
   p.group_chunk = g.group_chunk;
   p.chunk_info = g.chunk_info;
   p.status = status;
-  p.N = N;
-  p.K = K;
-  p.interleaved = w_interleaved ? 1 : 0;
-  p.fused = swiglu ? 1 : 0;
   p.early = early ? 1 : 0;
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -605,10 +773,10 @@ cudaError_t launch_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, co
     err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  const long long units_bound = chunks_bound(R_max, E) * (N / kBM);
+  const long long units_bound = chunks_bound(R_max, E) * (j0.N / kBM + (j1 ? j1->N / kBM : 0));
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
-  return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, tmB, p);
+  return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, tmB0, tmB1, p);
 }
 
 }  // namespace moe
