@@ -60,14 +60,14 @@ constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight s
 constexpr int kBBoxRows = 16;
 constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 224;       // warp 0: TMA, 1: MMA, 2-5: epilogue, 6: scale copies
+constexpr int kThreads = 288;       // warp 0: weights, 1: MMA, 2-5: epilogue, 6-7: scale copies, 8: tokens
 constexpr int kCtasPerSm = 2;
 constexpr int kSmemBytes = 114688;  // per CTA: two CTAs fit the SM's 228 KB (1 KB reserved each)
 constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
 constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: up values [64][33] floats
 constexpr int kXchBytes = 9216;                    // 64 * 33 * 4 rounded up to 1 KB
 constexpr int kUq = 8;                             // unit queue: producer -> MMA, scale copies, epilogue
-constexpr int kUqReaders = 1 + 1 + 128;
+constexpr int kUqReaders = 1 + 2 + 1 + 128;  // MMA thread, scale-copy threads, token loader, epilogue threads
 
 // One grouped GEMM over the routed rows: weights (tiled), token operand
 // (TMA map passed beside the arguments), token scales, output.
@@ -105,9 +105,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -153,9 +150,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
                                             uint32_t sfb, uint32_t accumulate) {
   asm volatile(
@@ -183,6 +177,9 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[3
       : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -224,6 +221,12 @@ struct Ctl {
 __device__ __forceinline__ void give_up(const Ctl& c) {
   *c.abort_flag = 1;
   atomicExch(c.status, (int)MOE_ERR_TIMEOUT);
+}
+
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const struct Ctl& c);
+// Bounded wait with the first poll inline (the common case: already complete).
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, const struct Ctl& c) {
+  return mbar_try_wait(bar, parity) || wait_phase(bar, parity, c);
 }
 
 // Bounded wait: false if this or another role gave up.
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   // barrier slots: full[16], empty[16], acc_full[2], acc_empty[2], drain, scales_ready[16], unit_done,
-  // xch_full, xch_free, drain2
+  // xch_full, xch_free, drain2, unit queue full/empty[8], drain3, token full[16]
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -305,10 +308,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t drain2_bar = bar0 + 8u * (3 * kMaxStages + 8);
   auto uqf_bar = [&](int i) { return bar0 + 8u * (3 * kMaxStages + 9 + i); };
   auto uqe_bar = [&](int i) { return bar0 + 8u * (3 * kMaxStages + 9 + kUq + i); };
-  // after the barriers (< 640 bytes): TMEM address, abort flag, unit queue
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 640);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 644);
-  volatile int* uq = reinterpret_cast<volatile int*>(smem + 704);
+  const uint32_t drain3_bar = bar0 + 8u * (3 * kMaxStages + 9 + 2 * kUq);
+  auto tfull_bar = [&](int s) { return bar0 + 8u * (3 * kMaxStages + 10 + 2 * kUq + s); };  // token operand landed
+  // after the barriers (< 768 bytes): TMEM address, abort flag, unit queue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 768);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 772);
+  volatile int* uq = reinterpret_cast<volatile int*>(smem + 832);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Programmatic dependent launch: this grid may start while the previous
@@ -345,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(sfr_bar(s), 1);
+      mbar_init(sfr_bar(s), 2);  // weight-scale and token-scale copies
+      mbar_init(tfull_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -353,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     mbar_init(drain_bar, 1);
     mbar_init(drain2_bar, 1);
+    mbar_init(drain3_bar, 1);
     mbar_init(udone_bar, 4 * 32);
     mbar_init(xfull_bar, 64);
     mbar_init(xfree_bar, 64);
@@ -388,11 +395,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   };
 
   if (warp == 0) {
-    // ============================ TMA producer ============================
+    // ========================= weight stream producer =========================
     // Units are taken in increasing order: with two jobs from a global
     // counter (every job-0 unit is claimed, by a running CTA, before any
     // job-1 unit, so a job-1 wait always ends however many CTAs are
     // resident), otherwise blockIdx.x, blockIdx.x + gridDim.x, ...
+    // This thread issues only the weight copies (one 18 KB bulk copy per
+    // stage); warp 8 issues the token copies: a thread issues a bulk copy
+    // every few hundred cycles whatever its size, so the two streams go out
+    // from two warps.
     if (lane == 0) {
       const bool dynamic = p.work_ctr != nullptr;
       int static_next = blockIdx.x;
@@ -420,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       const uint64_t stream_policy = policy_evict_first();
       // With p.early, the first unit's first weight stages go out before
-      // waiting for the previous kernel (they do not depend on it); the token
-      // rows and their scales follow once it has completed.
+      // waiting for the previous kernel (they do not depend on it).
       int cur = (total_units > 0) ? claim() : -1;
       int prefetched = 0;
       if (p.early) {
@@ -430,9 +440,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           for (int ks = 0; ks < un.nk && ks < stages; ++ks) {
             const int natoms = min(4, un.kc4 - 4 * ks);
             const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
-            mbar_expect_tx_only(full_bar(ks), wbytes);
+            mbar_expect_tx(full_bar(ks), wbytes);
             bulk_load_hint(sW + ks * kWStageBytes, un.w + (size_t)ks * kWStageBytes, wbytes, full_bar(ks),
                            stream_policy);
+            filled |= 1u << ks;
             ++prefetched;
           }
         }
@@ -444,70 +455,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (!push(cur)) { ok = false; break; }
         if (cur < 0) break;
         const Unit un = decode_unit(cur, p, U0, nt0, nt1);
-        const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
-        const int nbox = un.nmma / kBBoxRows;
-        // token rows + scales of stage ks into ring slot `slot` (pre: its
-        // weights were prefetched, so this is the stage's arrival)
-        auto issue_tokens = [&](int slot, int ks, bool pre) {
-          const int natoms = min(4, un.kc4 - 4 * ks);
-          const uint32_t fb = full_bar(slot);
-          if (pre) mbar_expect_tx(fb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(sB + slot * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, map, ks * kStageKBytes,
-                        un.row0 + b * kBBoxRows, fb);
-          bulk_load(sSFB + slot * kSfStageBytes, un.sfb + (size_t)ks * kSfStageBytes, natoms * kAtomBytes, fb);
-        };
-        // Job 1 reads h, which job 0 writes: its weights stream at once, its
-        // token copies wait until every job-0 tile of the chunk is done
-        // (pending stages, at most a ring's worth).
-        bool dep = un.job == 0;
-        int pend_n = 0, pend_ks = 0, pend_slot = 0, pend_issued = 0;
-        auto flush = [&]() {
-          for (int j = 0; j < pend_n; ++j) {
-            int slot = pend_slot + j;
-            if (slot >= stages) slot -= stages;
-            issue_tokens(slot, pend_ks + j, pend_issued + j < prefetched);
-          }
-          pend_n = 0;
-        };
         for (int ks = 0; ks < un.nk; ++ks, ++issued) {
-          if (pend_n == stages) {
-            // every slot waits for h: the next one cannot be refilled before it arrives.
-            // On a timeout the (in-bounds) token copies are still issued so that
-            // the slots' phases complete and the drain below ends.
-            const bool got = wait_count(p.chunk_done + un.chunk, nt0, ctl);
-            flush();
-            dep = true;
-            if (!got) { ok = false; break; }
-          }
-          const int natoms = min(4, un.kc4 - 4 * ks);
-          const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
-          const uint32_t tbytes = nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes;
-          const uint32_t fb = full_bar(stage);
           if (issued >= prefetched) {
-            if (!wait_phase(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
-            mbar_expect_tx(fb, wbytes + tbytes);
-            bulk_load_hint(sW + stage * kWStageBytes, un.w + (size_t)ks * kWStageBytes, wbytes, fb, stream_policy);
-          }
-          filled |= 1u << stage;
-          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-          if (!dep) {
-            if (pend_n == 0) { pend_ks = ks; pend_slot = stage; pend_issued = issued; }
-            ++pend_n;
-            if (ld_acquire(p.chunk_done + un.chunk) >= nt0) {
-              fence_proxy_async_global();
-              dep = true;
-              flush();
-            }
-          } else {
-            issue_tokens(stage, ks, issued < prefetched);
+            if (!wait_fast(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
+            const int natoms = min(4, un.kc4 - 4 * ks);
+            const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
+            mbar_expect_tx(full_bar(stage), wbytes);
+            bulk_load_hint(sW + stage * kWStageBytes, un.w + (size_t)ks * kWStageBytes, wbytes, full_bar(stage),
+                           stream_policy);
+            filled |= 1u << stage;
+            fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
           }
           if (++stage == stages) { stage = 0; phase ^= 1u; }
-        }
-        if (pend_n > 0) {
-          const bool got = wait_count(p.chunk_done + un.chunk, nt0, ctl);
-          flush();
-          if (!got) ok = false;
         }
         // the next unit is claimed once this one's copies are all issued (a
         // ring's worth of stages still in flight hides the atomic's latency);
@@ -524,11 +483,57 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
       }
     }
-  } else if (warp == 6) {
-    // ======================== scale copies into TMEM =======================
-    // Slot s's scale columns are rewritten only after the slot was refilled,
-    // i.e. after the MMAs that read them completed (empty[s]).
+  } else if (warp == 8) {
+    // ========================= token operand loader =========================
+    // Per stage: the token rows (TMA, 16-row boxes, 128B swizzle) and their
+    // scale atoms into the slot once it is free, completing tfull[s]. Job 1
+    // reads h, written by job 0: its copies wait until every job-0 tile of
+    // the chunk is done (the weights stream on meanwhile).
     if (lane == 0) {
+      if (p.early) pdl_wait();  // the token rows come from the previous kernel
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, fill_parity = 0;
+      bool ok = true;
+      while (ok) {
+        const int u = next_unit();
+        if (u < 0) { ok = u == -1; break; }
+        const Unit un = decode_unit(u, p, U0, nt0, nt1);
+        const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
+        const int nbox = un.nmma / kBBoxRows;
+        // On a timeout the (in-bounds) token copies are still issued, so that
+        // the slots' phases complete and the drain below ends.
+        if (un.job == 1 && !wait_count(p.chunk_done + un.chunk, nt0, ctl)) ok = false;
+        for (int ks = 0; ks < un.nk; ++ks) {
+          if (!wait_fast(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
+          const int natoms = min(4, un.kc4 - 4 * ks);
+          const uint32_t tb = tfull_bar(stage);
+          mbar_expect_tx(tb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, map, ks * kStageKBytes,
+                        un.row0 + b * kBBoxRows, tb);
+          bulk_load(sSFB + stage * kSfStageBytes, un.sfb + (size_t)ks * kSfStageBytes, natoms * kAtomBytes, tb);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < stages; ++s)
+          if (filled & (1u << s)) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(tfull_bar(s), (fill_parity >> s) & 1u) && clock64() - t0 < ctl.budget) {
+            }
+          }
+      }
+    }
+  } else if (warp == 6 || warp == 7) {
+    // ======================== scale copies into TMEM =======================
+    // Warp 6 copies the weight scales, warp 7 the token scales of every stage
+    // (two issuing threads: a single one's tcgen05 issue rate would pace the
+    // stage). Slot s's scale columns are rewritten only after the slot was
+    // refilled, i.e. after the MMAs that read them completed (empty[s]).
+    if (lane == 0) {
+      const bool tok = warp == 7;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -538,24 +543,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int K = u >= U0 ? p.j1.K : p.j0.K;
         const int nk = (K + 255) / 256, kc4 = K / 64;
         for (int ks = 0; ks < nk; ++ks) {
-          if (!wait_phase(full_bar(stage), phase, ctl)) { ok = false; break; }
+          if (!wait_fast(tok ? tfull_bar(stage) : full_bar(stage), phase, ctl)) { ok = false; break; }
           tc_fence_after();
           const int natoms = min(4, kc4 - 4 * ks);
-          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
-          const uint32_t sWs = sW + stage * kWStageBytes;
-          for (int a = 0; a < natoms; ++a) {
-            tc_cp_scales(sf_col + 4 * a, desc_scales(sWs + kATileBytes + a * kAtomBytes));
-            tc_cp_scales(sf_col + 16 + 4 * a, desc_scales(sSFB + stage * kSfStageBytes + a * kAtomBytes));
-          }
+          const uint32_t col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage + (tok ? 16 : 0));
+          const uint64_t src = desc_scales(tok ? sSFB + stage * kSfStageBytes : sW + stage * kWStageBytes + kATileBytes);
+          // atom a at +512 bytes: +32 in the descriptor's address field
+          for (int a = 0; a < natoms; ++a) tc_cp_scales(col + 4 * a, src + 32 * a);
           tc_commit(sfr_bar(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
         // wait for this thread's copies before TMEM is freed
-        tc_commit(drain2_bar);
+        const uint32_t db = tok ? drain3_bar : drain2_bar;
+        tc_commit(db);
         const long long t0 = clock64();
-        while (!mbar_try_wait(drain2_bar, 0) && clock64() - t0 < ctl.budget) {
+        while (!mbar_try_wait(db, 0) && clock64() - t0 < ctl.budget) {
         }
       }
     }
@@ -575,18 +579,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t idesc = idesc_nvf4(un.nmma);
         for (int ks = 0; ks < un.nk; ++ks) {
           // operands landed (full) and their scales are in tensor memory (scales ready)
-          if (!wait_phase(full_bar(stage), phase, ctl) || !wait_phase(sfr_bar(stage), phase, ctl)) {
+          if (!wait_fast(full_bar(stage), phase, ctl) || !wait_fast(tfull_bar(stage), phase, ctl) ||
+              !wait_fast(sfr_bar(stage), phase, ctl)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int natoms = min(4, un.kc4 - 4 * ks);
           const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
-          const uint32_t sWs = sW + stage * kWStageBytes;
-          for (int a = 0; a < natoms; ++a) {
-            const uint64_t adesc = desc_sw128(sWs + 32 * a);
-            const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes + 32 * a);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a, (ks | a) != 0);
+          // K step a (32 bytes along the 128-byte swizzled rows): +2 in the address field
+          const uint64_t adesc = desc_sw128(sW + stage * kWStageBytes);
+          const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes);
+          if (natoms == 4) {
+            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sf_col, sf_col + 16, ks != 0);
+            tc_mma_nvf4(d_tmem, adesc + 2, bdesc + 2, idesc, sf_col + 4, sf_col + 20, 1u);
+            tc_mma_nvf4(d_tmem, adesc + 4, bdesc + 4, idesc, sf_col + 8, sf_col + 24, 1u);
+            tc_mma_nvf4(d_tmem, adesc + 6, bdesc + 6, idesc, sf_col + 12, sf_col + 28, 1u);
+          } else {
+            for (int a = 0; a < natoms; ++a)
+              tc_mma_nvf4(d_tmem, adesc + 2 * a, bdesc + 2 * a, idesc, sf_col + 4 * a, sf_col + 16 + 4 * a,
+                          (ks | a) != 0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == stages) { stage = 0; phase ^= 1u; }
