@@ -10,7 +10,8 @@
  *
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers owned by the caller unless a comment says
- *     "host". The library allocates no device memory.
+ *     "host". The library allocates no device memory. Device buffers must be
+ *     16-byte aligned (MOE_ERR_INVALID otherwise).
  *   - bf16 tensors are passed as uint16_t bit patterns.
  *   - Work is enqueued on `stream` and runs asynchronously; nothing here
  *     synchronizes except moe_nvfp4_check_status.
@@ -19,7 +20,8 @@
  *     except MOE_ERR_CUDA (a launch failed part way).
  *   - Results are deterministic: the same inputs give bit-identical outputs,
  *     and a token's output does not depend on which other tokens share the
- *     batch (fixed expert order, no atomics in any reduction).
+ *     batch (fixed expert order; every sum runs in a fixed order, atomics
+ *     only hand out and count work).
  *
  * NVFP4 formats (page "Fusing the MoE layer's two grouped GEMMs is worth 4%",
  * table "Bytes decide it before the kernel runs": 0.5 + 1/16 byte/element)

@@ -42,6 +42,10 @@ int* status_ptr() {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Every device buffer the kernels read or write with vector accesses must be
+// 16-byte aligned; a null pointer passes here and is checked separately.
+bool misaligned(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 != 0; }
+
 bool groups_ok(const moe_groups_t* g) {
   return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->group_chunk &&
          g->chunk_info && g->row_slot && g->slot_row;
@@ -165,6 +169,7 @@ int moe_route_groups(const int32_t* topk_ids, int T, int k, int E, const moe_gro
 int moe_gather_rows(const uint16_t* x, int T, int H, const int32_t* topk_ids, int k, int E,
                     const moe_groups_t* groups, uint16_t* xg, cudaStream_t stream) {
   if (H <= 0 || H % 8 || (T > 0 && k > 0 && (!x || !xg))) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(xg)) return MOE_ERR_INVALID;
   const int st = moe_route_groups(topk_ids, T, k, E, groups, stream);
   if (st != MOE_OK || T * k == 0) return st;
   return status_of(launch_gather(x, H, k, T * k, *groups, xg, stream));
@@ -177,6 +182,7 @@ int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe
   if (K % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!rows || !packed || !sf) return MOE_ERR_INVALID;
+  if (misaligned(rows) || misaligned(packed) || misaligned(sf)) return MOE_ERR_INVALID;
   return status_of(launch_quantize(rows, 0, R_max, E, K, *groups, layout, packed, sf, stream));
 }
 
@@ -188,6 +194,7 @@ int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, cons
   if (H % 64) return MOE_ERR_SHAPE;
   if (T * k == 0) return MOE_OK;
   if (!x || !packed || !sf) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(packed) || misaligned(sf)) return MOE_ERR_INVALID;
   return status_of(launch_quantize(x, k, T * k, E, H, *groups, layout, packed, sf, stream));
 }
 
@@ -233,6 +240,7 @@ int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !h) return MOE_ERR_INVALID;
+  if (misaligned(d13) || misaligned(h)) return MOE_ERR_INVALID;
   return status_of(launch_swiglu(d13, R_max, E, I, *groups, MOE_SF_CHUNK32, g_gate_up, h, nullptr, nullptr, stream));
 }
 
@@ -243,6 +251,7 @@ int swiglu_quantize_grouped(const float* d13, int R_max, int I, int E, const moe
   if (I % 64) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
   if (!d13 || !g_gate_up || !packed || !sf) return MOE_ERR_INVALID;
+  if (misaligned(d13) || misaligned(packed) || misaligned(sf)) return MOE_ERR_INVALID;
   return status_of(launch_swiglu(d13, R_max, E, I, *groups, layout, g_gate_up, nullptr, packed, sf, stream));
 }
 
@@ -252,6 +261,7 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
   if (H % 4) return MOE_ERR_SHAPE;
   if (T == 0) return MOE_OK;
   if (!y || (k > 0 && (!d2 || !topk_ids || !topk_w || !g_down))) return MOE_ERR_INVALID;
+  if (misaligned(d2) || misaligned(y)) return MOE_ERR_INVALID;
   if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
   return status_of(launch_scatter(d2, H, topk_ids, topk_w, T, k, E, *groups, g_down, y, stream));
 }
@@ -269,6 +279,7 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (H % 128 || I % 128) return MOE_ERR_SHAPE;
   if (T == 0) return MOE_OK;
   if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(y)) return MOE_ERR_INVALID;
   if (!w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !w->g_down) return MOE_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(w->w13_tiled) % 16 || reinterpret_cast<uintptr_t>(w->w2_tiled) % 16)
     return MOE_ERR_INVALID;

@@ -68,6 +68,11 @@ def test_host_side_validation(native):
     assert native.moe_route_groups(16, 2, 2, 2000, ctypes.byref(g), s) == 1
     assert native.moe_route_groups(16, 2, 40, 8, ctypes.byref(g), s) == 1
     assert native.moe_scatter_add(16, 256, 16, 16, 2, 2, -1, ctypes.byref(g), 16, 16, s) == 1
+    # device buffers must be 16-byte aligned
+    assert native.moe_scatter_add(24, 256, 16, 16, 2, 2, 8, ctypes.byref(g), 16, 16, s) == 1
+    assert native.moe_scatter_add(16, 256, 16, 16, 2, 2, 8, ctypes.byref(g), 16, 40, s) == 1
+    assert native.nvfp4_quantize_rows(24, 8, 128, 4, ctypes.byref(g), 1, 16, 16, s) == 1
+    assert native.swiglu_grouped(16, 8, 128, 4, ctypes.byref(g), 16, 8, s) == 1
     w = _native.MoeWeights(8, 16, 16, 16, 16)
     assert native.moe_nvfp4_layer(16, 4, 200, 128, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
     assert native.moe_nvfp4_layer(16, 4, 256, 96, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
