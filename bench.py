@@ -32,7 +32,7 @@ METRIC = "MoE layer ms/step and weight-stream GB/s (% of HBM roofline) at M=1/8/
 FALLBACK_HBM_GBS = 6800.0
 N_ROUTINGS = 20
 GEMM_SRC = os.path.join(ROOT, "nvfp4_block_scaled_gather_gb300", "csrc", "nvfp4_gemm.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_w13_decode_m1_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "expert_gemms_decode_m1_traffic.txt")
 
 
 def expert_bytes(H, I):
@@ -46,12 +46,12 @@ def step_bytes(cfg, G, T):
     return G * expert_bytes(cfg.H, cfg.I) + 2 * T * cfg.H * 2 + T * cfg.k * 8 + 12 * cfg.E
 
 
-def w13_launch_bytes(cfg, G, R):
-    """Algorithmic bytes of one w13 grouped-GEMM launch (SwiGLU and the
-    requantization fused in its epilogue): the active experts' w13 (2I x H
-    e2m1 + scales), the NVFP4 activation rows and their scales, the NVFP4
-    h rows and their scales."""
-    return G * 2 * cfg.I * cfg.H * 9 // 16 + R * cfg.H * 9 // 16 + R * cfg.I * 9 // 16
+def gemms_launch_bytes(cfg, G, R):
+    """Algorithmic bytes of the layer's GEMM launch (w13 with SwiGLU and
+    requantization in its epilogue, then w2): the active experts' w13 and w2
+    (e2m1 + scales), the NVFP4 token rows and scales read, the NVFP4 h rows
+    and scales written and read back, the fp32 d2 rows written."""
+    return G * expert_bytes(cfg.H, cfg.I) + R * cfg.H * 9 // 16 + 2 * (R * cfg.I * 9 // 16) + R * cfg.H * 4
 
 
 def measured_peaks():
@@ -68,8 +68,8 @@ def measured_peaks():
 
 
 def recorded_traffic():
-    """ncu DRAM bytes per w13 launch (decode M=1), if recorded for the current
-    kernel source; None when absent or when the kernel changed since."""
+    """ncu DRAM bytes per GEMM launch (decode M=1), if recorded for the
+    current kernel source; None when absent or when the kernel changed since."""
     try:
         with open(GEMM_SRC, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
@@ -237,9 +237,10 @@ def gpu_bench(args, rank, world):
         hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
         hsf = torch.empty(N.sf_bytes(S, c.E, c.I, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
         d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
-        names = ["route", "gather_quantize", "gemm_w13", "gemm_w2", "scatter"]
+        gate = torch.zeros(N.expert_gemms_gate_bytes(S, c.E), dtype=torch.uint8, device=dev)  # zeroed once
+        names = ["route", "gather_quantize", "expert_gemms", "scatter"]
         acc = {n: [] for n in names}
-        w13_bytes = []
+        gemm_bytes = []
         for i in range(steps + 3):
             it = items[i % len(items)]
             T = it["T"]
@@ -252,18 +253,16 @@ def gpu_bench(args, rank, world):
             evs[1].record(stream)
             N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf)
             evs[2].record(stream)
-            N.nvfp4_grouped_gemm_swiglu(xq, xsf, G1, W.w13, W.g_gate_up, hq, hsf)
+            N.nvfp4_moe_expert_gemms(xq, xsf, G1, W, hq, hsf, d2, gate)
             evs[3].record(stream)
-            N.nvfp4_grouped_gemm(hq, hsf, G1, W.w2, d2)
-            evs[4].record(stream)
             N.moe_scatter_add(d2, it["ids"], it["tw"], c.E, G1, W.g_down, y)
-            evs[5].record(stream)
+            evs[4].record(stream)
             torch.cuda.synchronize()
             if i >= 3:
                 for j, n in enumerate(names):
                     acc[n].append(evs[j].elapsed_time(evs[j + 1]))
-                w13_bytes.append(w13_launch_bytes(c, it["G"], it["R"]))
-        return {n: statistics.mean(v) for n, v in acc.items()}, statistics.mean(w13_bytes)
+                gemm_bytes.append(gemms_launch_bytes(c, it["G"], it["R"]))
+        return {n: statistics.mean(v) for n, v in acc.items()}, statistics.mean(gemm_bytes)
 
     def time_e2e(c, items, steps):
         """Through the public call with host buffers: pinned H2D of x, ids and
@@ -326,9 +325,9 @@ def gpu_bench(args, rank, world):
     ms_step = total_ms / args.steps
     gbs = world * sum(byts) / (total_ms * 1e-3) / 1e9
 
-    stages, w13_bytes = time_stages(cfg, items, max(5, min(args.steps, 20)))
+    stages, gemm_bytes = time_stages(cfg, items, max(5, min(args.steps, 20)))
     peak, peak_kind = measured_peaks()
-    achieved = w13_bytes / (stages["gemm_w13"] * 1e-3) / 1e9
+    achieved = gemm_bytes / (stages["expert_gemms"] * 1e-3) / 1e9
     e2e_ms, e2e_bytes, h2d, d2h = time_e2e(cfg, items, max(5, min(args.steps, 20)))
     e2e_gbs = world * sum(e2e_bytes) / (sum(e2e_ms) * 1e-3) / 1e9
 
@@ -377,14 +376,14 @@ def gpu_bench(args, rank, world):
         "roof_frac": round(gbs / world / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "gemm_kernel (w13 grouped GEMM)",
+            "kernel": "gemm_kernel (w13 + SwiGLU/requantize, then w2: one launch)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic(),
-            "algorithmic_bytes_per_launch": round(w13_bytes),
+            "algorithmic_bytes_per_launch": round(gemm_bytes),
         },
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(statistics.mean(e2e_ms), 5),

@@ -49,6 +49,9 @@ _SIGS = {
                                    c_int, c_int, c_void_p, c_void_p]),
     "nvfp4_grouped_gemm_swiglu": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int,
                                           c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_expert_gemms_gate_bytes": (ctypes.c_size_t, [c_int, c_int]),
+    "nvfp4_moe_expert_gemms": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, ctypes.POINTER(MoeWeights),
+                                       c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
                                c_void_p]),
     "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
@@ -210,6 +213,19 @@ def nvfp4_grouped_gemm_swiglu(a_packed, a_sf, groups: Groups, w13: TiledWeight, 
            load().nvfp4_grouped_gemm_swiglu(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max,
                                             _ptr(w13.data), w13.E, w13.N // 2, K, _ptr(g_gate_up), _ptr(h_packed),
                                             _ptr(h_sf), _stream(stream)))
+
+
+def nvfp4_moe_expert_gemms(x_packed, x_sf, groups: Groups, W: "Weights", h_packed, h_sf, d2, gate, stream=None):
+    """Both grouped GEMMs in one launch (w13 + SwiGLU + requantize, then w2)."""
+    R_max = x_packed.shape[0]
+    _check("nvfp4_moe_expert_gemms",
+           load().nvfp4_moe_expert_gemms(_ptr(x_packed), _ptr(x_sf), ctypes.byref(groups.struct), R_max,
+                                         ctypes.byref(W.struct), W.H, W.I, _ptr(h_packed), _ptr(h_sf), _ptr(d2),
+                                         _ptr(gate), _stream(stream)))
+
+
+def expert_gemms_gate_bytes(R_max: int, E: int) -> int:
+    return load().moe_expert_gemms_gate_bytes(R_max, E)
 
 
 def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):

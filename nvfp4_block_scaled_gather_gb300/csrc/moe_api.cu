@@ -81,7 +81,7 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   w.hq = take(S * I / 2);
   w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
   w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
-  w.ngate = 1 + (int)chunks_bound((long long)S, E);
+  w.ngate = 2 + (int)chunks_bound((long long)S, E);
   w.gate = reinterpret_cast<int*>(take((size_t)w.ngate * sizeof(int)));
   w.bytes = off;
   return w;
@@ -232,6 +232,34 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
   const SwigluOut out{h_packed, h_sf, g_gate_up};
   const GemmJob job{a_packed, a_sf, w13_tiled, true, 2 * I, K, nullptr};
   return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, false, st, stream));
+}
+
+size_t moe_expert_gemms_gate_bytes(int R_max, int E) {
+  if (R_max < 0 || E <= 0) return 0;
+  return (size_t)(2 + chunks_bound(R_max, E)) * sizeof(int);
+}
+
+int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const moe_groups_t* groups, int R_max,
+                           const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed, uint8_t* h_sf, float* d2,
+                           void* gate, cudaStream_t stream) {
+  if (!w || !groups_ok(groups) || R_max < 0 || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
+    return MOE_ERR_INVALID;
+  if (H % 128 || I % 128) return MOE_ERR_SHAPE;
+  if ((long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!x_packed || !x_sf || !w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !h_packed || !h_sf || !d2 || !gate)
+    return MOE_ERR_INVALID;
+  if (misaligned(x_packed) || misaligned(x_sf) || misaligned(w->w13_tiled) || misaligned(w->w2_tiled) ||
+      misaligned(h_packed) || misaligned(h_sf) || misaligned(d2) || misaligned(gate))
+    return MOE_ERR_INVALID;
+  int* st = status_ptr();
+  if (!st) return MOE_ERR_CUDA;
+  const int E = w->E;
+  const SwigluOut swiglu{h_packed, h_sf, w->g_gate_up};
+  const GemmJob w13{x_packed, x_sf, w->w13_tiled, true, 2 * I, H, nullptr};
+  const GemmJob w2{h_packed, h_sf, w->w2_tiled, false, H, I, d2};
+  return status_of(
+      launch_grouped_gemm(*groups, R_max, E, w13, &swiglu, &w2, static_cast<int*>(gate), false, st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,

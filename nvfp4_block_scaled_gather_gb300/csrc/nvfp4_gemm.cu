@@ -88,6 +88,7 @@ struct GemmArgs {
   const float* g_gate_up;   // ... with the per-expert (gate, up) globals
   int* chunk_done;          // njobs == 2: job-0 tiles finished per chunk (zero at launch)
   int* work_ctr;            // njobs == 2: next unit to claim (zero at launch)
+  int* exit_ctr;            // njobs == 2: CTAs done; the last one zeroes the counters again
   const int32_t* counts;
   const int32_t* group_chunk;
   const int32_t* chunk_info;
@@ -711,6 +712,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && p.exit_ctr) {
+    // The last CTA out leaves the counters zero for the next launch: every
+    // other CTA has made its last claim and read its last chunk count.
+    __threadfence();
+    if (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1) {
+      for (int c = 0; c < nchunks; ++c) p.chunk_done[c] = 0;
+      *p.work_ctr = 0;
+      *p.exit_ctr = 0;
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
@@ -773,7 +784,8 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
     p.g_gate_up = swiglu->g_gate_up;
   }
   p.work_ctr = j1 ? gate : nullptr;
-  p.chunk_done = j1 ? gate + 1 : nullptr;
+  p.exit_ctr = j1 ? gate + 1 : nullptr;
+  p.chunk_done = j1 ? gate + 2 : nullptr;
   p.counts = g.counts;
   p.group_chunk = g.group_chunk;
   p.chunk_info = g.chunk_info;

@@ -324,6 +324,28 @@ def test_swiglu_requant_fused_equals_separate(small):
         assert torch.equal(p2[:R], st["hq"][:R]) and torch.equal(s2, st["hsf"])
 
 
+def test_expert_gemms_one_launch_equals_two(small):
+    """Both grouped GEMMs in one persistent launch (w2 units gated per chunk
+    on h) give the same h and d2 bits as the two launches run one after the
+    other; repeated calls agree (the work counters are re-zeroed per call)."""
+    E, x, ids, tw, W, *_ = small
+    st = run_stages(x, ids, tw, W, E)
+    dev = x.device
+    G = N.Groups(x.shape[0], ids.shape[1], E, dev)
+    N.moe_route_groups(ids, E, G)
+    R = st["groups"]["R"]
+    gate = torch.zeros(N.expert_gemms_gate_bytes(st["xq"].shape[0], E), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        hq = torch.zeros_like(st["hq"])
+        hsf = torch.zeros_like(st["hsf"])
+        d2 = torch.zeros_like(st["d2"])
+        N.nvfp4_moe_expert_gemms(st["xq"], st["xsf"], G, W, hq, hsf, d2, gate)
+        torch.cuda.synchronize()
+        assert torch.equal(hq[:R], st["hq"][:R]) and torch.equal(hsf, st["hsf"])
+        assert torch.equal(d2[:R], st["d2"][:R])
+    assert N.check_status() == 0
+
+
 def test_layer_determinism_and_batch_invariance(small):
     E, x, ids, tw, W, *_ = small
     layer = N.MoeLayer(W, x.shape[0], ids.shape[1])
