@@ -344,8 +344,9 @@ def gpu_bench(args, rank, world):
                                 "roof_frac": round(g2 / peak, 4),
                                 "mean_active_experts": statistics.mean(i["G"] for i in it2),
                                 "rows": statistics.mean(i["R"] for i in it2)}
-    # route, gather+quantize, the w13+w2 grouped GEMM (one persistent launch), scatter
-    launches_per_step = 4
+    # route, gather+quantize (one launch when T*k <= 32), the w13+w2 grouped GEMM (one
+    # persistent launch), scatter
+    launches_per_step = 3 if max(i["T"] for i in items) * cfg.k <= 32 else 4
     out = {
         "metric": METRIC,
         "value": round(gbs, 2),

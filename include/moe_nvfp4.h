@@ -168,6 +168,15 @@ int nvfp4_quantize_rows(const uint16_t* rows, int R_max, int K, int E, const moe
 int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, const moe_groups_t* groups,
                              int layout, uint8_t* packed, uint8_t* sf, cudaStream_t stream);
 
+/* a1 + a2 + a3 -- moe_route_gather_quantize: groups the T*k slots (as
+ * moe_route_groups) and writes the routed rows x[row_slot[r]/k, :] as NVFP4
+ * (packed [T*k, H/2], token scales in MOE_SF_CHUNK32). For T*k <= 32 (decode
+ * batches) it is one launch: one warp routes, the CTA quantizes; otherwise
+ * moe_route_groups then moe_gather_quantize_rows. Outputs are identical
+ * either way. H % 64 == 0. */
+int moe_route_gather_quantize(const int32_t* topk_ids, int T, int k, int E, const uint16_t* x, int H,
+                              const moe_groups_t* groups, uint8_t* packed, uint8_t* sf, cudaStream_t stream);
+
 /* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
  * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
  * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
@@ -242,17 +251,21 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
                     int T, int k, int E, const moe_groups_t* groups, const float* g_down,
                     uint16_t* y, cudaStream_t stream);
 
-/* Workspace bytes of moe_nvfp4_layer for these sizes (group metadata, NVFP4
- * activations and scales, fp32 GEMM outputs). */
+/* Workspace bytes of moe_nvfp4_layer for these sizes (the GEMM launch's work
+ * counters, group metadata, NVFP4 activations and scales, fp32 GEMM
+ * outputs). */
 size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I);
 
 /* The whole step a1..a8 on `stream`: route-group, gather+quantize, grouped
  * GEMM w13 with SwiGLU+requantize in its epilogue, grouped GEMM w2,
- * scatter-add (four kernels, each allowed to start while the previous one
- * finishes: programmatic dependent launch). x [T, H] bf16,
- * y [T, H] bf16 (overwritten). `workspace` is caller device memory of
- * ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I), 256-byte
- * aligned. H % 128 == 0, I % 128 == 0, k <= 32, E <= 1024. */
+ * scatter-add. Four launches for T*k > 32 (route, gather+quantize, both
+ * GEMMs in one persistent launch, scatter), three for decode-sized batches
+ * (T*k <= 32: route + gather + quantize in one). Each launch may start while
+ * the previous one finishes (programmatic dependent launch).
+ * x [T, H] bf16, y [T, H] bf16 (overwritten). `workspace` is caller device
+ * memory of ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I),
+ * 256-byte aligned (any contents). Calls sharing a workspace run in stream
+ * order. H % 128 == 0, I % 128 == 0, k <= 32, E <= 1024. */
 int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
                     const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
                     void* workspace, size_t ws_bytes, uint16_t* y, cudaStream_t stream);

@@ -49,6 +49,8 @@ _SIGS = {
                                    c_int, c_int, c_void_p, c_void_p]),
     "nvfp4_grouped_gemm_swiglu": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int,
                                           c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_route_gather_quantize": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_int, ctypes.POINTER(MoeGroups),
+                                          c_void_p, c_void_p, c_void_p]),
     "moe_expert_gemms_gate_bytes": (ctypes.c_size_t, [c_int, c_int]),
     "nvfp4_moe_expert_gemms": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, ctypes.POINTER(MoeWeights),
                                        c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -215,6 +217,14 @@ def nvfp4_grouped_gemm_swiglu(a_packed, a_sf, groups: Groups, w13: TiledWeight, 
                                             _ptr(h_sf), _stream(stream)))
 
 
+def moe_route_gather_quantize(topk_ids, x, E: int, groups: Groups, packed, sf, stream=None):
+    """Route + gather + quantize (one launch for T*k <= 32), MOE_SF_CHUNK32 scales."""
+    T, k = topk_ids.shape
+    _check("moe_route_gather_quantize",
+           load().moe_route_gather_quantize(_ptr(topk_ids), T, k, E, _ptr(x), x.shape[1],
+                                            ctypes.byref(groups.struct), _ptr(packed), _ptr(sf), _stream(stream)))
+
+
 def nvfp4_moe_expert_gemms(x_packed, x_sf, groups: Groups, W: "Weights", h_packed, h_sf, d2, gate, stream=None):
     """Both grouped GEMMs in one launch (w13 + SwiGLU + requantize, then w2)."""
     R_max = x_packed.shape[0]
@@ -313,7 +323,8 @@ class MoeLayer:
         import torch
         self.weights, self.k, self.T_max = weights, k, T_max
         n = moe_nvfp4_layer_workspace_size(T_max, k, weights.E, weights.H, weights.I)
-        self.workspace = torch.empty(n, dtype=torch.uint8, device=weights.w13.data.device)
+        # zeroed once: the step's work counters live here and every completed call leaves them zero
+        self.workspace = torch.zeros(n, dtype=torch.uint8, device=weights.w13.data.device)
 
     def __call__(self, x, topk_ids, topk_w, y=None, stream=None):
         import torch

@@ -44,6 +44,13 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 // E bounds the group count (grid size); CTAs past the routed blocks exit.
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
                             const moe_groups_t& g, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
+// a1 + a2 + a3 in one launch for S = T*k <= 32 slots (rows x[slot / k]),
+// token scales in MOE_SF_CHUNK32; same outputs as launch_route followed by
+// launch_quantize(x, k, ...).
+cudaError_t launch_route_quantize_small(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, int* zero,
+                                        int nzero, const uint16_t* x, int k, int K, uint8_t* packed, uint8_t* sf,
+                                        cudaStream_t s);
+constexpr int kSmallRouteSlots = 32;
 // h != nullptr: write bf16 h; otherwise packed/sf get the quantized h.
 cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,
                           const float* g_gate_up, uint16_t* h, uint8_t* packed, uint8_t* sf, cudaStream_t s);
@@ -90,7 +97,17 @@ struct GemmJob {
   int N, K;
   float* d;
 };
+// front != nullptr (small batches, S = T*k <= 32; early must be false):
+// every CTA routes the slots itself from topk_ids (which must be two or more
+// launches old) and, before waiting for the previous kernel (the
+// gather-quantize of these rows), prefetches into L2 the first weight stages
+// of the units the first claims hand out.
+struct SmallFront {
+  const int32_t* topk_ids;
+  int S;
+};
 cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
-                                const GemmJob* j1, int* gate, bool early, int* status, cudaStream_t s);
+                                const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
+                                cudaStream_t s);
 
 }  // namespace moe

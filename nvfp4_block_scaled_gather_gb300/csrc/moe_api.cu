@@ -74,6 +74,9 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
     off += align256(bytes);
     return p;
   };
+  const int nch = (int)chunks_bound((long long)S, E);
+  w.ngate = 2 + nch;
+  w.gate = reinterpret_cast<int*>(take((size_t)w.ngate * sizeof(int)));
   uint8_t* gmem = take(moe_groups_bytes(T, k, E));
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
@@ -81,8 +84,6 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   w.hq = take(S * I / 2);
   w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
   w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
-  w.ngate = 2 + (int)chunks_bound((long long)S, E);
-  w.gate = reinterpret_cast<int*>(take((size_t)w.ngate * sizeof(int)));
   w.bytes = off;
   return w;
 }
@@ -198,6 +199,23 @@ int moe_gather_quantize_rows(const uint16_t* x, int T, int H, int k, int E, cons
   return status_of(launch_quantize(x, k, T * k, E, H, *groups, layout, packed, sf, stream));
 }
 
+int moe_route_gather_quantize(const int32_t* topk_ids, int T, int k, int E, const uint16_t* x, int H,
+                              const moe_groups_t* groups, uint8_t* packed, uint8_t* sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || E <= 0 || E > kMaxExperts)
+    return MOE_ERR_INVALID;
+  if (H % 64) return MOE_ERR_SHAPE;
+  if ((long long)T * k > (1LL << 30)) return MOE_ERR_INVALID;
+  const int S = T * k;
+  if (S == 0) return status_of(launch_route(topk_ids, 0, E, *groups, stream));
+  if (!topk_ids || !x || !packed || !sf) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(packed) || misaligned(sf)) return MOE_ERR_INVALID;
+  if (S <= kSmallRouteSlots)
+    return status_of(launch_route_quantize_small(topk_ids, S, E, *groups, nullptr, 0, x, k, H, packed, sf, stream));
+  cudaError_t err = launch_route(topk_ids, S, E, *groups, stream);
+  if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, *groups, MOE_SF_CHUNK32, packed, sf, stream);
+  return status_of(err);
+}
+
 int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
                        const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
                        cudaStream_t stream) {
@@ -212,7 +230,7 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
   const GemmJob job{a_packed, a_sf, w_tiled, w_interleaved != 0, N, K, d};
-  return status_of(launch_grouped_gemm(*groups, R_max, E, job, nullptr, nullptr, nullptr, false, st, stream));
+  return status_of(launch_grouped_gemm(*groups, R_max, E, job, nullptr, nullptr, nullptr, nullptr, false, st, stream));
 }
 
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
@@ -231,7 +249,7 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
   if (!st) return MOE_ERR_CUDA;
   const SwigluOut out{h_packed, h_sf, g_gate_up};
   const GemmJob job{a_packed, a_sf, w13_tiled, true, 2 * I, K, nullptr};
-  return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, false, st, stream));
+  return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, nullptr, false, st, stream));
 }
 
 size_t moe_expert_gemms_gate_bytes(int R_max, int E) {
@@ -259,7 +277,8 @@ int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const m
   const GemmJob w13{x_packed, x_sf, w->w13_tiled, true, 2 * I, H, nullptr};
   const GemmJob w2{h_packed, h_sf, w->w2_tiled, false, H, I, d2};
   return status_of(
-      launch_grouped_gemm(*groups, R_max, E, w13, &swiglu, &w2, static_cast<int*>(gate), false, st, stream));
+      launch_grouped_gemm(*groups, R_max, E, w13, &swiglu, &w2, static_cast<int*>(gate), nullptr, false, st,
+                          stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -320,15 +339,28 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
   const int S = T * k;
-  cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate);
-  if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
+  // a1-a3: decode-sized batches (T*k <= 32) in one launch (route + gather + quantize), else
+  // route, then gather+quantize; either clears the GEMM launch's work counters. The GEMM
+  // launch starts on weights before the previous kernel ends: with a group table two launches
+  // old it claims units and streams them (early); for decode-sized batches it routes the
+  // slots itself from topk_ids and warms L2 with its first weight stages while it waits.
+  const bool small = S <= kSmallRouteSlots;
+  cudaError_t err;
+  if (small) {
+    err = launch_route_quantize_small(topk_ids, S, E, ws.groups, ws.gate, ws.ngate, x, k, H, ws.xq, ws.xsf, stream);
+  } else {
+    err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate);
+    if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
+  }
+  const SmallFront front{topk_ids, S};
   // a4 + a5 + a6 (w13 with SwiGLU and requantization in its epilogue) and a7
   // (w2) in one persistent launch; a w2 unit starts once its chunk's h is in
   const SwigluOut swiglu{ws.hq, ws.hsf, w->g_gate_up};
   const GemmJob w13{ws.xq, ws.xsf, w->w13_tiled, true, 2 * I, H, nullptr};
   const GemmJob w2{ws.hq, ws.hsf, w->w2_tiled, false, H, I, ws.d2};
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, true, st, stream);
+    err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, small ? &front : nullptr, !small, st,
+                              stream);
   if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
 }

@@ -16,6 +16,7 @@
 
 #include "internal.h"
 #include "nvfp4_codec.cuh"
+#include "ldcg.cuh"
 #include "pdl.cuh"
 
 namespace moe {
@@ -28,7 +29,7 @@ __device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, in
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(starts + mid) <= key) lo = mid; else hi = mid - 1;
+    if (ld_cg(starts + mid) <= key) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
   const int per = (S + 31) / 32;
   const int s0 = min(S, w * per), s1 = min(S, s0 + per);
   for (int s = s0 + lane; s < s1; s += 32) {
-    const int e = ids[s];
+    const int e = ld_cg(ids + s);
     if (e >= 0 && e < E) atomicAdd(&wc[w * E + e], 1);
   }
   __syncthreads();
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
   for (int c0 = s0; c0 < s1; c0 += 32) {
     const int s = c0 + lane;
     const bool in = s < s1;
-    const int e = in ? ids[s] : -1;
+    const int e = in ? ld_cg(ids + s) : -1;
     const bool ok = in && e >= 0 && e < E;
     const unsigned peers = __match_any_sync(~0u, ok ? e : -1);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -158,14 +159,14 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
                                                           moe_groups_t g, uint16_t* __restrict__ xg) {
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
-  const int R = __ldg(g.counts + 1);
+  const int R = ld_cg(g.counts + 1);
   const int per_row = H / 8;
   const long long total = (long long)R * per_row;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int r = (int)(i / per_row), j = (int)(i % per_row);
-    const int t = __ldg(g.row_slot + r) / k;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + j);
+    const int t = ld_cg(g.row_slot + r) / k;
+    const uint4 v = ld_cg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + j);
     reinterpret_cast<uint4*>(xg + (size_t)r * H)[j] = v;
   }
 }
@@ -227,26 +228,26 @@ struct RowBlock {
 
 __device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int layout, int blk) {
   if (layout == MOE_SF_CHUNK32) {  // one table read, same value in every thread
-    const int4 c = __ldg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
+    const int4 c = ld_cg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
     return RowBlock{c.x, c.y, c.z};
   }
   __shared__ int s_info[3];
   if (threadIdx.x == 0) {
-    const int G = __ldg(g.counts + 0);
+    const int G = ld_cg(g.counts + 0);
     const int gi = find_group(g.group_sf_block, G, blk);
-    const int m0 = (blk - __ldg(g.group_sf_block + gi)) * kRowsAtom;
-    const int r0 = __ldg(g.group_offsets + gi);
-    const int mg = __ldg(g.group_offsets + gi + 1) - r0;
+    const int m0 = (blk - ld_cg(g.group_sf_block + gi)) * kRowsAtom;
+    const int r0 = ld_cg(g.group_offsets + gi);
+    const int mg = ld_cg(g.group_offsets + gi + 1) - r0;
     s_info[0] = r0 + m0;
     s_info[1] = min(kRowsAtom, mg - m0);
-    s_info[2] = __ldg(g.group_expert + gi);
+    s_info[2] = ld_cg(g.group_expert + gi);
   }
   __syncthreads();
   return RowBlock{s_info[0], s_info[1], s_info[2]};
 }
 
 __device__ __forceinline__ int routed_blocks(const moe_groups_t& g, int layout) {
-  return __ldg(g.counts + (layout == MOE_SF_ATOM128 ? 3 : 4));
+  return ld_cg(g.counts + (layout == MOE_SF_ATOM128 ? 3 : 4));
 }
 
 constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K)
@@ -279,8 +280,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
     const int r = rb.row0 + m;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-      const int srow = src_k > 0 ? __ldg(g.row_slot + r) / src_k : r;
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)srow * K + kc0 + 4 * q));
+      const int srow = src_k > 0 ? ld_cg(g.row_slot + r) / src_k : r;
+      const uint2 u = ld_cg(reinterpret_cast<const uint2*>(src + (size_t)srow * K + kc0 + 4 * q));
       v[0] = bf16_to_f32(u.x & 0xFFFFu);
       v[1] = bf16_to_f32(u.x >> 16);
       v[2] = bf16_to_f32(u.y & 0xFFFFu);
@@ -290,6 +291,109 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
                         st.word(m, (kc0 + 4 * q) / 16));
   }
   st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
+}
+
+// ---------------------------------------------------------------------------
+// a1 + a2 + a3 for small batches (T*k <= 32 slots), one launch. Grid: (slot,
+// 1024-value column chunk). Warp 0 of every CTA routes the <= 32 slots (one
+// per lane): the same rows, groups and tables as route_kernel (rows ascend by
+// (expert, slot); with at most 32 rows no group has more than one 32-row chunk
+// or 128-row scale block); CTA (0, 0) writes the tables. CTA (r, c) then
+// gathers and quantizes column chunk c of routed row r into the 32-row-chunk
+// token layout exactly as quantize_kernel does; CTAs past the routed rows exit.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const int32_t* __restrict__ ids, int S, int E,
+                                                                        moe_groups_t g, int* __restrict__ zero,
+                                                                        int nzero, const uint16_t* __restrict__ x,
+                                                                        int k, int K, uint8_t* __restrict__ packed,
+                                                                        uint8_t* __restrict__ sf) {
+  pdl_wait();  // the previous kernel in the stream may still be running
+  pdl_trigger();
+  const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
+  if (lead)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+  __shared__ int s_src[32], s_chunk[32], s_m[32], s_cnt[32], s_R;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const bool in = lane < S;
+    const int e = in ? ld_cg(ids + lane) : -1;
+    const bool ok = in && e >= 0 && e < E;
+    const int key = ok ? e : 0x7fffffff;
+    const unsigned peers = __match_any_sync(~0u, key);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int n = __popc(peers);
+    const unsigned leaders = __ballot_sync(~0u, ok && rank == 0);
+    const int R = __popc(__ballot_sync(~0u, ok)), G = __popc(leaders);
+    int less = 0, gless = 0;  // rows and groups of lower experts
+    for (int j = 0; j < 32; ++j) {
+      const int kj = __shfl_sync(~0u, key, j);
+      if (kj < key) {
+        ++less;
+        gless += (leaders >> j) & 1u;
+      }
+    }
+    int mx = ok ? n : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(~0u, mx, o));
+    if (ok) {
+      const int row = less + rank;
+      s_src[row] = lane / k;
+      s_chunk[row] = gless;
+      s_m[row] = rank;
+      if (rank == 0) s_cnt[gless] = n;
+      if (lead) {
+        g.row_slot[row] = lane;
+        g.slot_row[lane] = row;
+        if (rank == 0) {
+          g.group_expert[gless] = e;
+          g.group_offsets[gless] = less;
+          g.group_sf_block[gless] = gless;
+          g.group_chunk[gless] = gless;
+          reinterpret_cast<int4*>(g.chunk_info)[gless] = make_int4(less, n, e, gless);
+        }
+      }
+    } else if (in && lead) {
+      g.slot_row[lane] = -1;
+    }
+    if (lane == 0) {
+      s_R = R;
+      if (lead) {
+        g.counts[0] = G;
+        g.counts[1] = R;
+        g.counts[2] = mx;
+        g.counts[3] = G;
+        g.counts[4] = G;
+        g.group_offsets[G] = R;
+        g.group_sf_block[G] = G;
+        g.group_chunk[G] = G;
+      }
+    }
+  }
+  __syncthreads();
+  const int r = blockIdx.x;
+  if (r >= s_R) return;
+  const int Kc = K / 16;
+  const int kc0 = blockIdx.y * kColsPerCta;
+  const int kcount = min(kColsPerCta, K - kc0);
+  const int c = s_chunk[r], m = s_m[r];
+  const ScaleTarget st{sf + (size_t)c * 128 * Kc, MOE_SF_CHUNK32, Kc};
+  const int lane = threadIdx.x & 31;
+  for (int base = (threadIdx.x & ~31); base < kcount / 4; base += blockDim.x) {
+    const int q = base + lane;
+    const bool active = q < kcount / 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      const uint2 u = ld_cg(reinterpret_cast<const uint2*>(x + (size_t)s_src[r] * K + kc0 + 4 * q));
+      v[0] = bf16_to_f32(u.x & 0xFFFFu);
+      v[1] = bf16_to_f32(u.x >> 16);
+      v[2] = bf16_to_f32(u.y & 0xFFFFu);
+      v[3] = bf16_to_f32(u.y >> 16);
+    }
+    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2,
+                        st.word(m, (kc0 + 4 * q) / 16));
+  }
+  // the chunk's first row also zeroes the words no row fills in these atoms
+  if (m == 0) st.zero_rest(kc0 / 64, kcount / 64, s_cnt[c]);
 }
 
 // ---------------------------------------------------------------------------
@@ -306,7 +410,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
   if (blk >= routed_blocks(g, layout)) return;
   const RowBlock rb = resolve_block(g, layout, blk);
   const int e = rb.expert;
-  const float gg = __ldg(g_gate_up + 2 * e), gu = __ldg(g_gate_up + 2 * e + 1);
+  const float gg = ld_cg(g_gate_up + 2 * e), gu = ld_cg(g_gate_up + 2 * e + 1);
   const int Kc = I / 16;
   const int kc0 = blockIdx.y * kColsPerCta;
   const int kcount = min(kColsPerCta, I - kc0);
@@ -323,8 +427,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
       const float* src = d13 + (size_t)r * 2 * I + kc0 + 4 * q;
-      const float4 a = __ldg(reinterpret_cast<const float4*>(src));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(src + I));
+      const float4 a = ld_cg(reinterpret_cast<const float4*>(src));
+      const float4 b = ld_cg(reinterpret_cast<const float4*>(src + I));
       const float ga[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int z = 0; z < 4; ++z) {
@@ -370,10 +474,10 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
     float coef = 0.0f;
     if (lane < k) {
       const int slot = t * k + lane;
-      const int e = __ldg(ids + slot);
+      const int e = ld_cg(ids + slot);
       if (e >= 0 && e < E) {
-        row = __ldg(g.slot_row + slot);
-        coef = __ldg(topk_w + slot) * __ldg(g_down + e);
+        row = ld_cg(g.slot_row + slot);
+        coef = ld_cg(topk_w + slot) * ld_cg(g_down + e);
       }
     }
     int rank = 0;
@@ -389,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
   const int n = s_n;
   for (int i = 0; i < n; ++i) {
     const float c = s_coef[i];
-    const float4 d = __ldg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i] * H + col));
+    const float4 d = ld_cg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i] * H + col));
     a0 = __fmaf_rn(c, d.x, a0);
     a1 = __fmaf_rn(c, d.y, a1);
     a2 = __fmaf_rn(c, d.z, a2);
@@ -416,7 +520,7 @@ __global__ void __launch_bounds__(kThreads) swizzle_kernel(const uint8_t* __rest
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int r = (int)(i / words), c4 = (int)(i % words);
-    const uint32_t v = r < N ? __ldg(reinterpret_cast<const uint32_t*>(linear + (size_t)r * Kc) + c4) : 0u;
+    const uint32_t v = r < N ? ld_cg(reinterpret_cast<const uint32_t*>(linear + (size_t)r * Kc) + c4) : 0u;
     *reinterpret_cast<uint32_t*>(out + sf_atom_offset(r, 4 * c4, Kc)) = v;
   }
 }
@@ -452,7 +556,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restric
       const int ks = (int)(ts % nk), t = (int)(ts / nk);
       const int col = ks * 128 + c * 16;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (col < rowb) v = __ldg(reinterpret_cast<const uint4*>(packed + (size_t)tile_src_row(t, r, il) * rowb + col));
+      if (col < rowb) v = ld_cg(reinterpret_cast<const uint4*>(packed + (size_t)tile_src_row(t, r, il) * rowb + col));
       *reinterpret_cast<uint4*>(out + (size_t)ts * 18432 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     } else {
       const long long j = i - chunks;
@@ -462,7 +566,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const uint8_t* __restric
       const int m = (wi >> 2) + 32 * (wi & 3);
       const int col = (4 * ks + a) * 4;  // first scale column of this atom
       uint32_t v = 0u;
-      if (col < Kc) v = __ldg(reinterpret_cast<const uint32_t*>(sf_linear + (size_t)tile_src_row(t, m, il) * Kc + col));
+      if (col < Kc) v = ld_cg(reinterpret_cast<const uint32_t*>(sf_linear + (size_t)tile_src_row(t, m, il) * Kc + col));
       *reinterpret_cast<uint32_t*>(out + (size_t)ts * 18432 + 16384 + a * 512 + wi * 4) = v;
     }
   }
@@ -495,6 +599,15 @@ cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, in
                             int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kColsPerCta - 1) / kColsPerCta);
   return launch_pdl(quantize_kernel, grid, dim3(kThreads), 0, s, src, src_k, K, g, layout, packed, sf);
+}
+
+cudaError_t launch_route_quantize_small(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, int* zero,
+                                        int nzero, const uint16_t* x, int k, int K, uint8_t* packed, uint8_t* sf,
+                                        cudaStream_t s) {
+  if (S > 32 || k <= 0 || K % 64) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)S, (K + kColsPerCta - 1) / kColsPerCta);
+  return launch_pdl(route_quantize_small_kernel, grid, dim3(kThreads), 0, s, topk_ids, S, E, g, zero,
+                    zero ? nzero : 0, x, k, K, packed, sf);
 }
 
 cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_groups_t& g, int layout,

@@ -46,6 +46,7 @@
 
 #include "internal.h"
 #include "nvfp4_codec.cuh"
+#include "ldcg.cuh"
 #include "pdl.cuh"
 
 namespace moe {
@@ -67,6 +68,8 @@ constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
 constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: up values [64][33] floats
 constexpr int kXchBytes = 9216;                    // 64 * 33 * 4 rounded up to 1 KB
 constexpr int kUq = 8;                             // unit queue: producer -> MMA, scale copies, epilogue
+constexpr int kHeader = 2048;                      // barriers, TMEM address, queue, small-batch routing tables
+constexpr int kSmallSlots = 32;                    // inline routing: at most 32 slots
 constexpr int kUqReaders = 1 + 2 + 1 + 128;  // MMA thread, scale-copy threads, token loader, epilogue threads
 
 // One grouped GEMM over the routed rows: weights (tiled), token operand
@@ -89,6 +92,14 @@ struct GemmArgs {
   int* chunk_done;          // njobs == 2: job-0 tiles finished per chunk (zero at launch)
   int* work_ctr;            // njobs == 2: next unit to claim (zero at launch)
   int* exit_ctr;            // njobs == 2: CTAs done; the last one zeroes the counters again
+  // small != 0: T*k <= 32 slots; every CTA routes them itself (one warp)
+  // from topk_ids, written two or more launches back, and before waiting for
+  // the previous kernel (the gather-quantize of these rows) prefetches into
+  // L2 the first weight stages of unit blockIdx.x, the unit the first claims
+  // hand out; claims and everything else follow the wait (early must be 0)
+  int small;
+  const int32_t* topk_ids;  // [S] slots
+  int S, E;
   const int32_t* counts;
   const int32_t* group_chunk;
   const int32_t* chunk_info;
@@ -140,6 +151,9 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -269,14 +283,15 @@ struct Unit {
   const uint8_t* sfb;  // the chunk's first token-scale block
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int U0, int nt0, int nt1) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int U0, int nt0, int nt1, const int4* tab) {
   Unit un;
   un.job = u >= U0 ? 1 : 0;
   const int v = un.job ? u - U0 : u;
   const int ntl = un.job ? nt1 : nt0;
   un.chunk = v / ntl;
   un.nt = v - un.chunk * ntl;
-  const int4 c = __ldg(reinterpret_cast<const int4*>(p.chunk_info) + un.chunk);  // row0, rows, expert, group
+  // row0, rows, expert, group: the small mode's table in shared memory, else the group metadata
+  const int4 c = tab ? tab[un.chunk] : ld_cg(reinterpret_cast<const int4*>(p.chunk_info) + un.chunk);
   un.row0 = c.x;
   un.nvalid = c.y;
   un.expert = c.z;
@@ -287,6 +302,36 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int U0, in
   un.w = (un.job ? p.j1.w_tiled : p.j0.w_tiled) + ((size_t)un.expert * ntl + un.nt) * un.nk * kWStageBytes;
   un.sfb = (un.job ? p.j1.a_sf : p.j0.a_sf) + (size_t)un.chunk * un.kc4 * kAtomBytes;
   return un;
+}
+
+// Small mode: warp 0 routes the <= 32 slots, one per lane, into this CTA's
+// tables: rows ascend by (expert, slot), one group and one 32-row chunk per
+// expert, the same rows and chunks moe_route_groups produces.
+__device__ __noinline__ void small_route(const GemmArgs& p, int lane, int4* s_tab, int* s_meta) {
+  const bool in = lane < p.S;
+  const int e = in ? ld_cg(p.topk_ids + lane) : -1;
+  const bool ok = in && e >= 0 && e < p.E;
+  const int key = ok ? e : 0x7fffffff;
+  const unsigned peers = __match_any_sync(~0u, key);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  const int n = __popc(peers);
+  const unsigned leaders = __ballot_sync(~0u, ok && rank == 0);
+  int less = 0, gless = 0;  // rows and groups of lower experts
+  for (int j = 0; j < kSmallSlots; ++j) {
+    const int kj = __shfl_sync(~0u, key, j);
+    if (kj < key) {
+      ++less;
+      gless += (leaders >> j) & 1u;
+    }
+  }
+  int mx = ok ? n : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(~0u, mx, o));
+  if (ok && rank == 0) s_tab[gless] = make_int4(less, n, e, gless);
+  if (lane == 0) {
+    s_meta[0] = __popc(leaders);
+    s_meta[2] = mx;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -315,38 +360,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 768);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 772);
   volatile int* uq = reinterpret_cast<volatile int*>(smem + 832);
+  int4* s_tab = reinterpret_cast<int4*>(smem + 1024);     // small mode: chunk table [32]
+  int* s_meta = reinterpret_cast<int*>(smem + 1536);      // small mode: G, -, max rows per group
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Programmatic dependent launch: this grid may start while the previous
-  // kernel in the stream still runs. Everything it reads must be complete
-  // first; with p.early the group metadata and the weights are two or more
-  // launches old (complete), and only the token operand waits below.
-  if (!p.early) {
-    pdl_wait();
-    pdl_trigger();
-  }
-
-  // ---- schedule shape, identical on every thread ----
-  const int G = __ldg(p.counts + 0);
-  const int maxmg = __ldg(p.counts + 2);
-  const int nchunks = G > 0 ? __ldg(p.group_chunk + G) : 0;
-  const int nt0 = p.j0.N / kBM;
-  const int nt1 = p.njobs > 1 ? p.j1.N / kBM : 1;
-  const int U0 = nchunks * nt0;
-  const int total_units = U0 + (p.njobs > 1 ? nchunks * nt1 : 0);
-  const bool has_xch = p.fused0 != 0;
-  const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
-  const int acc_cols = max(32, tn);
-  const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
-  const int avail = kSmemBytes - 1024 - 1024 - (has_xch ? kXchBytes : 0);
-  int stages = min(kMaxStages, avail / stage_bytes);
-  stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
-  // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, token scales, exchange
-  const uint32_t sW = smem_u32(smem + 1024);
-  const uint32_t sB = sW + (uint32_t)stages * kWStageBytes;
-  const uint32_t sSFB = sB + (uint32_t)stages * tn * kStageKBytes;
-  float* xch = reinterpret_cast<float*>(smem + 1024 + (size_t)stages * stage_bytes);
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -383,6 +400,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.wait_budget};
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel in the stream still runs. Everything it reads must be complete
+  // first; with p.early the group metadata and the weights are two or more
+  // launches old (complete), and only the token operand waits below.
+  if (p.small) {
+    // Route the <= 32 slots in warp 0 of every CTA (one slot per lane).
+    if (warp == 0) small_route(p, lane, s_tab, s_meta);
+    __syncthreads();
+  } else if (!p.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  const int4* tab = p.small ? s_tab : nullptr;
+  // ---- schedule shape, identical on every thread ----
+  const int G = p.small ? s_meta[0] : ld_cg(p.counts + 0);
+  const int maxmg = p.small ? s_meta[2] : ld_cg(p.counts + 2);
+  const int nchunks = p.small ? G : (G > 0 ? ld_cg(p.group_chunk + G) : 0);
+  const int nt0 = p.j0.N / kBM;
+  const int nt1 = p.njobs > 1 ? p.j1.N / kBM : 1;
+  const int U0 = nchunks * nt0;
+  const int total_units = U0 + (p.njobs > 1 ? nchunks * nt1 : 0);
+  const bool has_xch = p.fused0 != 0;
+  const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
+  const int acc_cols = max(32, tn);
+  const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
+  const int avail = kSmemBytes - 1024 - kHeader - (has_xch ? kXchBytes : 0);
+  int stages = min(kMaxStages, avail / stage_bytes);
+  stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
+  // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, token scales, exchange
+  const uint32_t sW = smem_u32(smem + kHeader);
+  const uint32_t sB = sW + (uint32_t)stages * kWStageBytes;
+  const uint32_t sSFB = sB + (uint32_t)stages * tn * kStageKBytes;
+  if (p.small) {
+    // the first claims hand out units 0 .. gridDim.x - 1: warm L2 with this
+    // CTA's share of their first stages while the rows are still being quantized
+    if (threadIdx.x == 0 && (int)blockIdx.x < total_units) {
+      const Unit un = decode_unit(blockIdx.x, p, U0, nt0, nt1, tab);
+      for (int ks = 0; ks < un.nk && ks < stages; ++ks)
+        prefetch_l2(un.w + (size_t)ks * kWStageBytes, kATileBytes + min(4, un.kc4 - 4 * ks) * kAtomBytes);
+    }
+    pdl_wait();
+    pdl_trigger();
+  }
+  float* xch = reinterpret_cast<float*>(smem + kHeader + (size_t)stages * stage_bytes);
+
+
   // The producer hands every role the same unit sequence through the queue:
   // unit ids, then -1. Returns the next unit, -1 at the end, -2 on a timeout.
   int q_idx = 0;
@@ -437,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       int prefetched = 0;
       if (p.early) {
         if (cur >= 0) {
-          const Unit un = decode_unit(cur, p, U0, nt0, nt1);
+          const Unit un = decode_unit(cur, p, U0, nt0, nt1, tab);
           for (int ks = 0; ks < un.nk && ks < stages; ++ks) {
             const int natoms = min(4, un.kc4 - 4 * ks);
             const uint32_t wbytes = kATileBytes + natoms * kAtomBytes;
@@ -455,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       while (ok) {
         if (!push(cur)) { ok = false; break; }
         if (cur < 0) break;
-        const Unit un = decode_unit(cur, p, U0, nt0, nt1);
+        const Unit un = decode_unit(cur, p, U0, nt0, nt1, tab);
         for (int ks = 0; ks < un.nk; ++ks, ++issued) {
           if (issued >= prefetched) {
             if (!wait_fast(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
@@ -487,45 +550,51 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   } else if (warp == 8) {
     // ========================= token operand loader =========================
     // Per stage: the token rows (TMA, 16-row boxes, 128B swizzle) and their
-    // scale atoms into the slot once it is free, completing tfull[s]. Job 1
-    // reads h, written by job 0: its copies wait until every job-0 tile of
-    // the chunk is done (the weights stream on meanwhile).
-    if (lane == 0) {
-      if (p.early) pdl_wait();  // the token rows come from the previous kernel
-      int stage = 0;
-      uint32_t phase = 0, filled = 0, fill_parity = 0;
-      bool ok = true;
-      while (ok) {
-        const int u = next_unit();
-        if (u < 0) { ok = u == -1; break; }
-        const Unit un = decode_unit(u, p, U0, nt0, nt1);
-        const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
-        const int nbox = un.nmma / kBBoxRows;
-        // On a timeout the (in-bounds) token copies are still issued, so that
-        // the slots' phases complete and the drain below ends.
-        if (un.job == 1 && !wait_count(p.chunk_done + un.chunk, nt0, ctl)) ok = false;
-        for (int ks = 0; ks < un.nk; ++ks) {
-          if (!wait_fast(empty_bar(stage), phase ^ 1u, ctl)) { ok = false; break; }
-          const int natoms = min(4, un.kc4 - 4 * ks);
-          const uint32_t tb = tfull_bar(stage);
+    // scale atoms into the slot once it is free, completing tfull[s]. Job 1 reads
+    // h, written by job 0: its copies wait until every job-0 tile of the
+    // chunk is done (the weights stream on meanwhile).
+    if (p.early && lane == 0) pdl_wait();  // the token rows come from the previous kernel
+    int stage = 0;
+    uint32_t phase = 0, filled = 0, fill_parity = 0;
+    bool ok = true;
+    while (ok) {
+      int u = 0;
+      if (lane == 0) u = next_unit();
+      u = __shfl_sync(~0u, u, 0);
+      if (u < 0) { ok = u == -1; break; }
+      const Unit un = decode_unit(u, p, U0, nt0, nt1, tab);
+      const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
+      const int nbox = un.nmma / kBBoxRows;
+      // On a timeout the (in-bounds) token copies are still issued, so that
+      // the slots' phases complete and the drain below ends.
+      int dep = 1;
+      if (un.job == 1 && lane == 0) dep = wait_count(p.chunk_done + un.chunk, nt0, ctl) ? 1 : 0;
+      if (!__shfl_sync(~0u, dep, 0)) ok = false;
+      for (int ks = 0; ks < un.nk; ++ks) {
+        int got = 0;
+        if (lane == 0) got = wait_fast(empty_bar(stage), phase ^ 1u, ctl) ? 1 : 0;
+        if (!__shfl_sync(~0u, got, 0)) { ok = false; break; }
+        const int natoms = min(4, un.kc4 - 4 * ks);
+        const uint32_t tb = tfull_bar(stage);
+        if (lane == 0) {
           mbar_expect_tx(tb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, map, ks * kStageKBytes,
                         un.row0 + b * kBBoxRows, tb);
           bulk_load(sSFB + stage * kSfStageBytes, un.sfb + (size_t)ks * kSfStageBytes, natoms * kAtomBytes, tb);
-          filled |= 1u << stage;
-          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
+        filled |= 1u << stage;
+        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) {
-        for (int s = 0; s < stages; ++s)
-          if (filled & (1u << s)) {
-            const long long t0 = clock64();
-            while (!mbar_try_wait(tfull_bar(s), (fill_parity >> s) & 1u) && clock64() - t0 < ctl.budget) {
-            }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < stages; ++s)
+        if (filled & (1u << s)) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(tfull_bar(s), (fill_parity >> s) & 1u) && clock64() - t0 < ctl.budget) {
           }
-      }
+        }
     }
   } else if (warp == 6 || warp == 7) {
     // ======================== scale copies into TMEM =======================
@@ -573,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       while (ok) {
         const int u = next_unit();
         if (u < 0) { ok = u == -1; break; }
-        const Unit un = decode_unit(u, p, U0, nt0, nt1);
+        const Unit un = decode_unit(u, p, U0, nt0, nt1, tab);
         if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * acc_cols);
@@ -627,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     while (true) {
       const int u = next_unit();
       if (u < 0) break;
-      const Unit un = decode_unit(u, p, U0, nt0, nt1);
+      const Unit un = decode_unit(u, p, U0, nt0, nt1, tab);
       if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
@@ -664,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           mbar_arrive(xfull_bar);
         } else {
           if (!wait_phase(xfull_bar, xph, ctl)) break;
-          const float gg = __ldg(p.g_gate_up + 2 * un.expert), gu = __ldg(p.g_gate_up + 2 * un.expert + 1);
+          const float gg = ld_cg(p.g_gate_up + 2 * un.expert), gu = ld_cg(p.g_gate_up + 2 * un.expert + 1);
           uint8_t* hp = p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 + quad * 16 + (lane >> 1);
 #pragma unroll
           for (int j = 0; j < kTokChunk; ++j) {
@@ -758,7 +827,9 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t r
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
-                                const GemmJob* j1, int* gate, bool early, int* status, cudaStream_t s) {
+                                const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
+                                cudaStream_t s) {
+  if (front && (early || front->S > kSmallSlots || front->S < 1)) return cudaErrorInvalidValue;
   CUtensorMap tmB0, tmB1;
   if (!make_map(&tmB0, j0.a_packed, (uint64_t)j0.K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
   if (j1 && !make_map(&tmB1, j1->a_packed, (uint64_t)j1->K / 2, (uint64_t)R_max, kBBoxRows))
@@ -791,6 +862,12 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
   p.chunk_info = g.chunk_info;
   p.status = status;
   p.early = early ? 1 : 0;
+  if (front) {
+    p.small = 1;
+    p.topk_ids = front->topk_ids;
+    p.S = front->S;
+    p.E = E;
+  }
   p.wait_budget = 2000000000LL;
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)

@@ -324,6 +324,52 @@ def test_swiglu_requant_fused_equals_separate(small):
         assert torch.equal(p2[:R], st["hq"][:R]) and torch.equal(s2, st["hsf"])
 
 
+@pytest.mark.parametrize("T,k,E,pattern", [(1, 8, 288, "topk"), (4, 8, 288, "topk"), (2, 8, 16, "topk"),
+                                           (8, 4, 8, "one_expert"), (4, 8, 64, "unused"), (3, 2, 4, "all_unused"),
+                                           (5, 8, 288, "topk"), (32, 1, 288, "one_expert")])
+def test_route_gather_quantize_small_path(cuda, T, k, E, pattern):
+    """T*k <= 32 takes the one-launch path (one warp routes, the CTA
+    quantizes); its group tables, packed rows and token scales equal those of
+    moe_route_groups + moe_gather_quantize_rows byte for byte. T*k = 40 runs
+    the two-launch path inside the same entry point."""
+    H = 256
+    g = torch.Generator().manual_seed(T * 131 + k * 7 + E)
+    if pattern == "topk":
+        ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    elif pattern == "one_expert":
+        ids = torch.full((T, k), 3, dtype=torch.int32)
+    elif pattern == "unused":
+        ids = torch.randint(-2, E + 3, (T, k), generator=g, dtype=torch.int32)
+    else:
+        ids = torch.full((T, k), -1, dtype=torch.int32)
+    if pattern == "one_expert" and k > 1:
+        ids[:, 1:] = torch.arange(1, k, dtype=torch.int32) + 3
+    x = (torch.randn(T, H, generator=g) * 3).to(torch.bfloat16).to(cuda)
+    ids = ids.to(cuda)
+    S = T * k
+    outs = []
+    for one_launch in (True, False):
+        G = N.Groups(T, k, E, cuda)
+        xq = torch.full((S, H // 2), 0xAB, dtype=torch.uint8, device=cuda)
+        xsf = torch.full((N.sf_bytes(S, E, H, N.SF_CHUNK32),), 0xCD, dtype=torch.uint8, device=cuda)
+        if one_launch:
+            N.moe_route_gather_quantize(ids, x, E, G, xq, xsf)
+        else:
+            N.moe_route_groups(ids, E, G)
+            N.moe_gather_quantize_rows(x, k, G, xq, xsf)
+        torch.cuda.synchronize()
+        h = G.host()
+        nbytes = h["chunks"] * (H // 64) * 512
+        outs.append((h, xq[:h["R"]].cpu(), xsf[:nbytes].cpu()))
+    (h1, q1, s1), (h2, q2, s2) = outs
+    for key in ("G", "R", "max_mg", "blocks", "chunks"):
+        assert h1[key] == h2[key], key
+    for key in ("group_offsets", "group_expert", "group_sf_block", "group_chunk", "chunk_info", "row_slot",
+                "slot_row"):
+        assert torch.equal(h1[key], h2[key]), key
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
 def test_expert_gemms_one_launch_equals_two(small):
     """Both grouped GEMMs in one persistent launch (w2 units gated per chunk
     on h) give the same h and d2 bits as the two launches run one after the
@@ -343,6 +389,31 @@ def test_expert_gemms_one_launch_equals_two(small):
         torch.cuda.synchronize()
         assert torch.equal(hq[:R], st["hq"][:R]) and torch.equal(hsf, st["hsf"])
         assert torch.equal(d2[:R], st["d2"][:R])
+    assert N.check_status() == 0
+
+
+def test_back_to_back_calls_share_a_workspace(small):
+    """Layer calls queued back to back (no host sync) on one workspace,
+    alternating the one-launch small-batch front end (T*k <= 32) and the
+    general one (route, then gather+quantize): every call's output equals the
+    same call run alone. Kernels start before the one they depend on ends
+    (programmatic dependent launch), so a read of an earlier kernel's output
+    that could hit a stale cached line shows up here."""
+    E, x, ids, tw, W, *_ = small
+    cases = {n: (x[:n].contiguous(), ids[:n].contiguous(), tw[:n].contiguous()) for n in (3, 40)}
+    refs = {n: N.MoeLayer(W, n, ids.shape[1])(*c).clone() for n, c in cases.items()}
+    torch.cuda.synchronize()
+    ws = torch.zeros(N.moe_nvfp4_layer_workspace_size(40, ids.shape[1], E, W.H, W.I), dtype=torch.uint8,
+                     device=x.device)
+    outs = []
+    for _ in range(5):
+        for n in (40, 3, 3, 40, 3):
+            y = torch.empty_like(cases[n][0])
+            N.moe_nvfp4_layer(*cases[n], W, ws, y)
+            outs.append((n, y))
+    torch.cuda.synchronize()
+    for n, y in outs:
+        assert torch.equal(y.view(torch.int16), refs[n].view(torch.int16)), n
     assert N.check_status() == 0
 
 
