@@ -54,6 +54,23 @@ def gemms_launch_bytes(cfg, G, R):
     return G * expert_bytes(cfg.H, cfg.I) + R * cfg.H * 9 // 16 + 2 * (R * cfg.I * 9 // 16) + R * cfg.H * 4
 
 
+def max_over_ranks(value, dist_mod, device):
+    """The largest of every rank's value (a replica run's time is its slowest
+    rank's); the value itself when not distributed."""
+    if not dist_mod:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, bytes_per_rank, total_ms):
+    """Whole-job GB/s of `world` replicas that each moved bytes_per_rank in
+    the slowest rank's total_ms."""
+    return world * bytes_per_rank / (total_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -316,14 +333,9 @@ def gpu_bench(args, rank, world):
     ms, byts = time_layer(cfg, items, args.steps, args.warmup, sampler, graph=not args.eager)
     clocks = sampler.stop()
     ms_eager, _ = time_layer(cfg, items, max(10, min(args.steps, 40)), 3, graph=False)
-    if dist:
-        t = torch.tensor([sum(ms)], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    else:
-        total_ms = sum(ms)
+    total_ms = max_over_ranks(sum(ms), dist, dev)
     ms_step = total_ms / args.steps
-    gbs = world * sum(byts) / (total_ms * 1e-3) / 1e9
+    gbs = replica_throughput(world, sum(byts), total_ms)
 
     stages, gemm_bytes = time_stages(cfg, items, max(5, min(args.steps, 20)))
     peak, peak_kind = measured_peaks()
