@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // claiming earlier would let a CTA hoard units behind a job-1 wait
         cur = claim();
       }
-      if (!ok) {
+      if (!ok || *abort_flag) {  // this role, or another, gave up: nothing of ours may be in flight at exit
         // let every copy this thread issued land before the CTA exits
         for (int s = 0; s < stages; ++s)
           if (filled & (1u << s)) {
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (++stage == stages) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && lane == 0) {
+    if ((!ok || *abort_flag) && lane == 0) {  // as above
       for (int s = 0; s < stages; ++s)
         if (filled & (1u << s)) {
           const long long t0 = clock64();
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok || *abort_flag) {  // this role, or another, gave up: nothing of ours may be in flight at exit
         // wait for this thread's copies before TMEM is freed
         const uint32_t db = tok ? drain3_bar : drain2_bar;
         tc_commit(db);
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) {
+      if (!ok || *abort_flag) {  // this role, or another, gave up: nothing of ours may be in flight at exit
         // wait for every MMA issued so far before TMEM is freed
         tc_commit(drain_bar);
         const long long t0 = clock64();

@@ -392,6 +392,36 @@ def test_expert_gemms_one_launch_equals_two(small):
     assert N.check_status() == 0
 
 
+def test_bounded_wait_reports_timeout_and_the_context_survives(small):
+    """Failure detection without a fault: start the two-GEMM launch's claim
+    counter past every w13 unit, so no chunk's h is ever published and every
+    w2 unit's wait runs out (about a second of clock64). The kernel records
+    MOE_ERR_TIMEOUT, lets its own copies land, frees tensor memory and
+    returns; moe_nvfp4_check_status reports it once, and the next call on the
+    same context and counters is correct again."""
+    E, x, ids, tw, W, *_ = small
+    st = run_stages(x, ids, tw, W, E)
+    dev = x.device
+    G = N.Groups(x.shape[0], ids.shape[1], E, dev)
+    N.moe_route_groups(ids, E, G)
+    chunks = G.host()["chunks"]
+    R = st["groups"]["R"]
+    S = st["xq"].shape[0]
+    gate = torch.zeros(N.expert_gemms_gate_bytes(S, E) // 4, dtype=torch.int32, device=dev)
+    assert N.check_status() == 0
+    gate[0] = chunks * (2 * W.I // 128)          # claims start at the first w2 unit
+    hq, hsf, d2 = torch.zeros_like(st["hq"]), torch.zeros_like(st["hsf"]), torch.zeros_like(st["d2"])
+    N.nvfp4_moe_expert_gemms(st["xq"], st["xsf"], G, W, hq, hsf, d2, gate)
+    torch.cuda.synchronize()
+    assert N.check_status() == 4                  # MOE_ERR_TIMEOUT, read and cleared
+    assert N.check_status() == 0
+    assert int(gate.abs().sum()) == 0             # the last CTA out left the counters zero
+    N.nvfp4_moe_expert_gemms(st["xq"], st["xsf"], G, W, hq, hsf, d2, gate)
+    torch.cuda.synchronize()
+    assert torch.equal(hq[:R], st["hq"][:R]) and torch.equal(d2[:R], st["d2"][:R])
+    assert N.check_status() == 0
+
+
 def test_back_to_back_calls_share_a_workspace(small):
     """Layer calls queued back to back (no host sync) on one workspace,
     alternating the one-launch small-batch front end (T*k <= 32) and the
