@@ -254,7 +254,7 @@ def gpu_bench(args, rank, world):
         hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
         hsf = torch.empty(N.sf_bytes(S, c.E, c.I, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
         d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
-        gate = torch.zeros(N.expert_gemms_gate_bytes(S, c.E), dtype=torch.uint8, device=dev)  # zeroed once
+        gate = torch.zeros(N.expert_gemms_gate_bytes(S, c.E, c.I), dtype=torch.uint8, device=dev)  # zeroed once
         names = ["route", "gather_quantize", "expert_gemms", "scatter"]
         acc = {n: [] for n in names}
         gemm_bytes = []

@@ -209,20 +209,21 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
 /* a4 .. a7 in one persistent launch -- both grouped GEMMs of the layer: the
  * w13 GEMM with SwiGLU and requantization in its epilogue (as
  * nvfp4_grouped_gemm_swiglu, writing h_packed/h_sf) and the w2 GEMM reading
- * that h (as nvfp4_grouped_gemm into d2 [R_max, H] fp32). The w2 work of a
- * 32-row chunk starts when all w13 tiles of that chunk have written h, so
- * w2's weights stream while w13 finishes. This is the launch
+ * that h (as nvfp4_grouped_gemm into d2 [R_max, H] fp32). Each 256-wide K
+ * stage of a 32-row chunk's w2 work starts once the four w13 tiles writing
+ * those h features are done, so w2's weights stream, and its first stages
+ * run, while w13 finishes. This is the launch
  * moe_nvfp4_layer makes between quantization and the scatter-add; the pages
  * ran the two GEMMs as separate launches (second page, "Fusing the MoE
  * layer's two grouped GEMMs is worth 4%").
  * x_packed/x_sf: NVFP4 token rows [R_max, H/2] and MOE_SF_CHUNK32 scales.
- * gate: moe_expert_gemms_gate_bytes(R_max, E) bytes of device scratch for
+ * gate: moe_expert_gemms_gate_bytes(R_max, E, I) bytes of device scratch for
  * the launch's work counters. Zero it once before the first call; a call
  * that completes leaves it zero. After an error (e.g. MOE_ERR_TIMEOUT from
  * moe_nvfp4_check_status) zero it again. Calls sharing a gate must not run
  * concurrently.
  * H % 128 == 0, I % 128 == 0. */
-size_t moe_expert_gemms_gate_bytes(int R_max, int E);
+size_t moe_expert_gemms_gate_bytes(int R_max, int E, int I);
 int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const moe_groups_t* groups, int R_max,
                            const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed, uint8_t* h_sf,
                            float* d2, void* gate, cudaStream_t stream);

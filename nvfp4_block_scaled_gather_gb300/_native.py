@@ -51,7 +51,7 @@ _SIGS = {
                                           c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_route_gather_quantize": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_int, ctypes.POINTER(MoeGroups),
                                           c_void_p, c_void_p, c_void_p]),
-    "moe_expert_gemms_gate_bytes": (ctypes.c_size_t, [c_int, c_int]),
+    "moe_expert_gemms_gate_bytes": (ctypes.c_size_t, [c_int, c_int, c_int]),
     "nvfp4_moe_expert_gemms": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, ctypes.POINTER(MoeWeights),
                                        c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
@@ -234,8 +234,8 @@ def nvfp4_moe_expert_gemms(x_packed, x_sf, groups: Groups, W: "Weights", h_packe
                                          _ptr(gate), _stream(stream)))
 
 
-def expert_gemms_gate_bytes(R_max: int, E: int) -> int:
-    return load().moe_expert_gemms_gate_bytes(R_max, E)
+def expert_gemms_gate_bytes(R_max: int, E: int, I: int) -> int:
+    return load().moe_expert_gemms_gate_bytes(R_max, E, I)
 
 
 def swiglu_grouped(d13, groups: Groups, g_gate_up, h, stream=None):

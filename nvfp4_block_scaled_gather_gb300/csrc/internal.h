@@ -76,14 +76,18 @@ cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzle
 // swiglu_grouped followed by nvfp4_quantize_rows; job 0's d is not written.
 // j1 != nullptr: job 1 runs in the same launch and may read what job 0
 // wrote: a job-1 unit of a 32-row chunk starts its token loads once all of
-// job 0's tiles of that chunk are done. gate holds 2 + chunks_bound(R_max, E)
-// ints, zero at launch: the unit claim counter, the count of finished CTAs,
-// then the per-chunk counts of finished job-0 tiles. The last CTA to finish
-// zeroes them again, so a launch that completes leaves gate ready for the next.
+// job 0's tiles writing that stage's features are done. gate holds
+// gate_ints(R_max, E, K1) ints, zero at launch: the unit claim counter, the
+// count of finished CTAs, then per (chunk, job-1 K stage of 256) the count of
+// finished job-0 tiles. The last CTA to finish zeroes them again, so a launch
+// that completes leaves gate ready for the next.
 // early: the group metadata, gate and the weights were written two or more
 // launches back (true inside moe_nvfp4_layer), so the GEMM may read them and
 // start streaming weights before the previous kernel has finished.
 // status: device word that records a wait timeout (MOE_ERR_TIMEOUT).
+inline long long gate_ints(long long R_max, long long E, long long K1) {
+  return 2 + chunks_bound(R_max, E) * ((K1 + 255) / 256);
+}
 struct SwigluOut {
   uint8_t* packed;
   uint8_t* sf;

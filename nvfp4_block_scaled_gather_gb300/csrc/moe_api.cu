@@ -74,8 +74,7 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
     off += align256(bytes);
     return p;
   };
-  const int nch = (int)chunks_bound((long long)S, E);
-  w.ngate = 2 + nch;
+  w.ngate = (int)gate_ints((long long)S, E, I);
   w.gate = reinterpret_cast<int*>(take((size_t)w.ngate * sizeof(int)));
   uint8_t* gmem = take(moe_groups_bytes(T, k, E));
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
@@ -252,9 +251,9 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
   return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, nullptr, false, st, stream));
 }
 
-size_t moe_expert_gemms_gate_bytes(int R_max, int E) {
-  if (R_max < 0 || E <= 0) return 0;
-  return (size_t)(2 + chunks_bound(R_max, E)) * sizeof(int);
+size_t moe_expert_gemms_gate_bytes(int R_max, int E, int I) {
+  if (R_max < 0 || E <= 0 || I <= 0) return 0;
+  return (size_t)gate_ints(R_max, E, I) * sizeof(int);
 }
 
 int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const moe_groups_t* groups, int R_max,

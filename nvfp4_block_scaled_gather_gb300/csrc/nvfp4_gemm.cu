@@ -89,7 +89,8 @@ struct GemmArgs {
   uint8_t* h_packed;        // ... NVFP4 h [R_max, N0/4] ...
   uint8_t* h_sf;            // ... and its token scales (MOE_SF_CHUNK32, K = N0/2) ...
   const float* g_gate_up;   // ... with the per-expert (gate, up) globals
-  int* chunk_done;          // njobs == 2: job-0 tiles finished per chunk (zero at launch)
+  int* chunk_done;          // njobs == 2: per (chunk, job-1 K stage), job-0 tiles of that stage's h
+                            // features finished (zero at launch)
   int* work_ctr;            // njobs == 2: next unit to claim (zero at launch)
   int* exit_ctr;            // njobs == 2: CTAs done; the last one zeroes the counters again
   // small != 0: T*k <= 32 slots; every CTA routes them itself (one warp)
@@ -258,21 +259,37 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl
   }
 }
 
-// Bounded wait until another CTA's counter reaches target (acquire), then a
-// proxy fence so that this thread's TMA reads see what those CTAs wrote.
-__device__ __noinline__ bool wait_count(const int* ctr, int target, const Ctl& c) {
+// Warp-wide: how many stages from `ks` on are ready, i.e. their counters
+// (stage i: ctr[i] >= min(4, kc4 - 4 i)) have reached their targets. Lane l
+// polls stage ks + l with an acquire load, so one L2 round trip covers every
+// remaining stage; waits (bounded) until stage ks is ready, then a warp
+// barrier and a proxy fence make what the counters published visible to
+// lane 0's TMA reads. Returns the first stage not known ready (> ks), or -1
+// if the wait gave up.
+__device__ __noinline__ int ready_stages(const int* ctr, int ks, int nk, int kc4, int lane, const Ctl& c) {
   const long long t0 = clock64();
-  while (ld_acquire(ctr) < target) {
-    if (*c.abort_flag) return false;
-    if (clock64() - t0 > c.budget) {
-      give_up(c);
-      return false;
+  while (true) {
+    const int i = ks + lane;
+    bool sat = true;
+    if (i < nk) sat = ld_acquire(ctr + i) >= min(4, kc4 - 4 * i);
+    const unsigned m = __ballot_sync(~0u, sat);
+    if (m & 1u) {
+      __syncwarp();                // each lane's acquire is ordered before lane 0's copies
+      fence_proxy_async_global();
+      const int run = (~m) ? __ffs(~m) - 1 : 32;  // leading ready stages
+      return min(nk, ks + run);
     }
+    int stop = 0;
+    if (lane == 0) {
+      if (*c.abort_flag) stop = 1;
+      else if (clock64() - t0 > c.budget) { give_up(c); stop = 1; }
+    }
+    if (__shfl_sync(~0u, stop, 0)) return -1;
     __nanosleep(128);
   }
-  fence_proxy_async_global();
-  return true;
 }
+
+
 
 // One unit of work: 32-row chunk `chunk` of a group against 128-row weight
 // tile `nt` of the group's expert, for job 0 (units [0, U0)) or job 1. The
@@ -421,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int nt1 = p.njobs > 1 ? p.j1.N / kBM : 1;
   const int U0 = nchunks * nt0;
   const int total_units = U0 + (p.njobs > 1 ? nchunks * nt1 : 0);
+  const int nk1 = p.njobs > 1 ? (p.j1.K + 255) / 256 : 1;  // job-1 K stages (dependency counters per chunk)
   const bool has_xch = p.fused0 != 0;
   const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
   const int acc_cols = max(32, tn);
@@ -567,14 +585,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int nbox = un.nmma / kBBoxRows;
       // On a timeout the (in-bounds) token copies are still issued, so that
       // the slots' phases complete and the drain below ends.
-      int dep = 1;
-      if (un.job == 1 && lane == 0) dep = wait_count(p.chunk_done + un.chunk, nt0, ctl) ? 1 : 0;
-      if (!__shfl_sync(~0u, dep, 0)) ok = false;
+      int ready = un.job == 1 ? 0 : un.nk;  // stages whose token operand is known to be written
       for (int ks = 0; ks < un.nk; ++ks) {
         int got = 0;
         if (lane == 0) got = wait_fast(empty_bar(stage), phase ^ 1u, ctl) ? 1 : 0;
         if (!__shfl_sync(~0u, got, 0)) { ok = false; break; }
         const int natoms = min(4, un.kc4 - 4 * ks);
+        // job 1's K stage ks is h features [256 ks, 256 ks + 256): the job-0
+        // tiles 4 ks .. 4 ks + natoms - 1 of the chunk write them
+        if (ks >= ready) {
+          ready = ready_stages(p.chunk_done + (size_t)un.chunk * un.nk, ks, un.nk, un.kc4, lane, ctl);
+          if (ready < 0) { ok = false; ready = un.nk; }
+        }
         const uint32_t tb = tfull_bar(stage);
         if (lane == 0) {
           mbar_expect_tx(tb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
@@ -772,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_arrive(udone_bar);
         if (et == 0) {
           if (!wait_phase(udone_bar, uph, ctl)) break;
-          red_release_add(p.chunk_done + un.chunk, 1);
+          red_release_add(p.chunk_done + (size_t)un.chunk * nk1 + un.nt / 4, 1);  // tile nt: h features 64 nt ..
         }
         uph ^= 1u;
       }
@@ -786,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // other CTA has made its last claim and read its last chunk count.
     __threadfence();
     if (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1) {
-      for (int c = 0; c < nchunks; ++c) p.chunk_done[c] = 0;
+      for (int c = 0; c < nchunks * nk1; ++c) p.chunk_done[c] = 0;
       *p.work_ctr = 0;
       *p.exit_ctr = 0;
     }

@@ -380,7 +380,7 @@ def test_expert_gemms_one_launch_equals_two(small):
     G = N.Groups(x.shape[0], ids.shape[1], E, dev)
     N.moe_route_groups(ids, E, G)
     R = st["groups"]["R"]
-    gate = torch.zeros(N.expert_gemms_gate_bytes(st["xq"].shape[0], E), dtype=torch.uint8, device=dev)
+    gate = torch.zeros(N.expert_gemms_gate_bytes(st["xq"].shape[0], E, W.I), dtype=torch.uint8, device=dev)
     for _ in range(3):
         hq = torch.zeros_like(st["hq"])
         hsf = torch.zeros_like(st["hsf"])
@@ -407,7 +407,7 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(small):
     chunks = G.host()["chunks"]
     R = st["groups"]["R"]
     S = st["xq"].shape[0]
-    gate = torch.zeros(N.expert_gemms_gate_bytes(S, E) // 4, dtype=torch.int32, device=dev)
+    gate = torch.zeros(N.expert_gemms_gate_bytes(S, E, W.I) // 4, dtype=torch.int32, device=dev)
     assert N.check_status() == 0
     gate[0] = chunks * (2 * W.I // 128)          # claims start at the first w2 unit
     hq, hsf, d2 = torch.zeros_like(st["hq"]), torch.zeros_like(st["hsf"]), torch.zeros_like(st["d2"])
