@@ -21,12 +21,12 @@
 //    every 128-row tile and 256-value K stage, 16 KB of e2m1 bytes already in
 //    the 128-byte-swizzled shared-memory image followed by the 2 KB of e4m3
 //    scale atoms, so a stage is one contiguous 18 KB bulk copy.
-//  * Warp roles: warp 0 issues the weight bulk copies (L2 evict-first), a TMA
-//    load of the token rows (128B-swizzled) and a bulk copy of their scale
-//    atoms into an mbarrier ring; warp 6 copies each stage's scales into
-//    tensor memory (tcgen05.cp); warp 1 issues tcgen05.mma.kind::mxf4nvf4
-//    (scale vector 16) into a double-buffered TMEM accumulator; warps 2-5
-//    drain TMEM (tcgen05.ld).
+//  * Warp roles: warp 0 issues the weight bulk copies (L2 evict-first) into an
+//    mbarrier ring; warp 8 copies the token rows (into the 128-byte swizzle)
+//    and their scale atoms with 16-byte cp.async copies from all its lanes;
+//    warps 6 and 7 copy each stage's scales into tensor memory (tcgen05.cp);
+//    warp 1 issues tcgen05.mma.kind::mxf4nvf4 (scale vector 16) into a
+//    double-buffered TMEM accumulator; warps 2-5 drain TMEM (tcgen05.ld).
 //  * Epilogue either writes fp32 rows, or (w13 in the layer) applies SwiGLU
 //    with the per-half globals and requantizes h to NVFP4 right there, so the
 //    fp32 gate|up product never reaches HBM. For that the w13 tiles hold 64
@@ -39,8 +39,6 @@
 // each output column of the MMA depends only on its own token.
 #include <cstdint>
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +56,6 @@ constexpr int kAtomBytes = 512;     // one scale atom: 128 rows x 4 scales (64 K
 constexpr int kATileBytes = kBM * kStageKBytes;  // 16 KB
 constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
 constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
-constexpr int kBBoxRows = 16;
 constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 288;       // warp 0: weights, 1: MMA, 2-5: epilogue, 6-7: scale copies, 8: tokens
@@ -72,10 +69,11 @@ constexpr int kHeader = 2048;                      // barriers, TMEM address, qu
 constexpr int kSmallSlots = 32;                    // inline routing: at most 32 slots
 constexpr int kUqReaders = 1 + 2 + 1 + 128;  // MMA thread, scale-copy threads, token loader, epilogue threads
 
-// One grouped GEMM over the routed rows: weights (tiled), token operand
-// (TMA map passed beside the arguments), token scales, output.
+// One grouped GEMM over the routed rows: weights (tiled), token operand,
+// token scales, output.
 struct Job {
   const uint8_t* w_tiled;
+  const uint8_t* a_packed;  // token rows [R_max, K/2], NVFP4
   const uint8_t* a_sf;      // token scales, MOE_SF_CHUNK32, K wide
   float* d;                 // plain epilogue: fp32 rows [R_max, N]
   int N, K;
@@ -133,16 +131,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
+// 16-byte copy global -> shared through L2 only (the source may have been
+// written by another CTA or the previous kernel).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+// One arrival on the barrier once all of this thread's earlier cp.async
+// copies have landed (counts against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Orders shared memory written through the generic proxy (cp.async, plain
+// stores), as seen by this thread, before its later async-proxy reads
+// (tcgen05.mma and tcgen05.cp operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // Bulk copy with an L2 policy (weights are read once per step: evict first).
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
@@ -205,14 +209,15 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Orders this thread's view of global memory (after an acquire) before its
-// later async-proxy (TMA, bulk copy) reads.
+// later reads through another proxy.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// that TMA writes: rows of 128 bytes, 8-row groups 1024 bytes apart
-// (stride byte offset), descriptor version 1, swizzle mode 2 (128B).
+// (16-byte piece c of row r at piece c ^ (r % 8)): rows of 128 bytes, 8-row
+// groups 1024 bytes apart (stride byte offset), descriptor version 1,
+// swizzle mode 2 (128B).
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
@@ -263,9 +268,8 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl
 // (stage i: ctr[i] >= min(4, kc4 - 4 i)) have reached their targets. Lane l
 // polls stage ks + l with an acquire load, so one L2 round trip covers every
 // remaining stage; waits (bounded) until stage ks is ready, then a warp
-// barrier and a proxy fence make what the counters published visible to
-// lane 0's TMA reads. Returns the first stage not known ready (> ks), or -1
-// if the wait gave up.
+// barrier makes what the counters published visible to every lane's copies.
+// Returns the first stage not known ready (> ks), or -1 if the wait gave up.
 __device__ __noinline__ int ready_stages(const int* ctr, int ks, int nk, int kc4, int lane, const Ctl& c) {
   const long long t0 = clock64();
   while (true) {
@@ -274,7 +278,7 @@ __device__ __noinline__ int ready_stages(const int* ctr, int ks, int nk, int kc4
     if (i < nk) sat = ld_acquire(ctr + i) >= min(4, kc4 - 4 * i);
     const unsigned m = __ballot_sync(~0u, sat);
     if (m & 1u) {
-      __syncwarp();                // each lane's acquire is ordered before lane 0's copies
+      __syncwarp();                // each lane's acquire is ordered before every lane's copies
       fence_proxy_async_global();
       const int run = (~m) ? __ffs(~m) - 1 : 32;  // leading ready stages
       return min(nk, ks + run);
@@ -352,7 +356,7 @@ __device__ __noinline__ void small_route(const GemmArgs& p, int lane, int4* s_ta
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, GemmArgs p) {
+    gemm_kernel(GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sfr_bar(s), 2);  // weight-scale and token-scale copies
-      mbar_init(tfull_bar(s), 1);
+      mbar_init(tfull_bar(s), 32);  // one cp.async arrival per token-loader lane
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -567,13 +571,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else if (warp == 8) {
     // ========================= token operand loader =========================
-    // Per stage: the token rows (TMA, 16-row boxes, 128B swizzle) and their
-    // scale atoms into the slot once it is free, completing tfull[s]. Job 1 reads
-    // h, written by job 0: its copies wait until every job-0 tile of the
-    // chunk is done (the weights stream on meanwhile).
-    if (p.early && lane == 0) pdl_wait();  // the token rows come from the previous kernel
+    // Per stage, once the slot is free: the stage's 128 bytes of each valid
+    // token row, stored in the 128-byte swizzle the MMA reads, and the rows'
+    // scale atoms, as 16-byte cp.async copies spread over the warp's lanes;
+    // each lane's copies make one of tfull[s]'s 32 arrivals. (A bulk or TMA
+    // copy costs its issuing thread a few hundred cycles; these cost a load
+    // instruction.) Rows past the chunk's valid rows are not copied: they only
+    // feed accumulator columns the epilogue never reads. Job 1 reads h,
+    // written by job 0: the copies of its K stage ks wait until the job-0
+    // tiles that write those h features are done (the weights stream on
+    // meanwhile).
+    if (p.early) pdl_wait();  // the token rows come from the previous kernel
     int stage = 0;
-    uint32_t phase = 0, filled = 0, fill_parity = 0;
+    uint32_t phase = 0;
     bool ok = true;
     while (ok) {
       int u = 0;
@@ -581,10 +591,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       u = __shfl_sync(~0u, u, 0);
       if (u < 0) { ok = u == -1; break; }
       const Unit un = decode_unit(u, p, U0, nt0, nt1, tab);
-      const CUtensorMap* map = un.job ? &tmB1 : &tmB0;
-      const int nbox = un.nmma / kBBoxRows;
-      // On a timeout the (in-bounds) token copies are still issued, so that
-      // the slots' phases complete and the drain below ends.
+      const int K = un.job ? p.j1.K : p.j0.K;
+      const uint8_t* rows = (un.job ? p.j1.a_packed : p.j0.a_packed) + (size_t)un.row0 * (K / 2);
       int ready = un.job == 1 ? 0 : un.nk;  // stages whose token operand is known to be written
       for (int ks = 0; ks < un.nk; ++ks) {
         int got = 0;
@@ -595,29 +603,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // tiles 4 ks .. 4 ks + natoms - 1 of the chunk write them
         if (ks >= ready) {
           ready = ready_stages(p.chunk_done + (size_t)un.chunk * un.nk, ks, un.nk, un.kc4, lane, ctl);
-          if (ready < 0) { ok = false; ready = un.nk; }
+          if (ready < 0) { ok = false; break; }
         }
-        const uint32_t tb = tfull_bar(stage);
-        if (lane == 0) {
-          mbar_expect_tx(tb, nbox * kBBoxRows * kStageKBytes + natoms * kAtomBytes);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(sB + stage * tn * kStageKBytes + b * kBBoxRows * kStageKBytes, map, ks * kStageKBytes,
-                        un.row0 + b * kBBoxRows, tb);
-          bulk_load(sSFB + stage * kSfStageBytes, un.sfb + (size_t)ks * kSfStageBytes, natoms * kAtomBytes, tb);
+        // row r's 16-byte piece c (2 per 64-value K atom) goes to piece c ^ (r % 8) of the row
+        const uint32_t dst = sB + (uint32_t)(stage * tn * kStageKBytes);
+        const int per_row = 2 * natoms;
+        const uint8_t* src = rows + (size_t)ks * kStageKBytes;
+        for (int i = lane; i < un.nvalid * per_row; i += 32) {
+          const int r = i / per_row, c = i - r * per_row;
+          cp_async16(dst + (uint32_t)(r * kStageKBytes + ((c ^ (r & 7)) << 4)), src + (size_t)r * (K / 2) + c * 16);
         }
-        filled |= 1u << stage;
-        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        const uint32_t sdst = sSFB + (uint32_t)(stage * kSfStageBytes);
+        const uint8_t* ssrc = un.sfb + (size_t)ks * kSfStageBytes;
+        for (int i = lane; i < natoms * (kAtomBytes / 16); i += 32) cp_async16(sdst + (uint32_t)(i * 16), ssrc + i * 16);
+        cp_async_arrive(tfull_bar(stage));
         if (++stage == stages) { stage = 0; phase ^= 1u; }
       }
     }
-    if ((!ok || *abort_flag) && lane == 0) {  // as above
-      for (int s = 0; s < stages; ++s)
-        if (filled & (1u << s)) {
-          const long long t0 = clock64();
-          while (!mbar_try_wait(tfull_bar(s), (fill_parity >> s) & 1u) && clock64() - t0 < ctl.budget) {
-          }
-        }
-    }
+    // this role, or another, gave up: let every copy of this warp land before the CTA exits
+    if (!ok || *abort_flag) cp_async_wait_all();
   } else if (warp == 6 || warp == 7) {
     // ======================== scale copies into TMEM =======================
     // Warp 6 copies the weight scales, warp 7 the token scales of every stage
@@ -637,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int ks = 0; ks < nk; ++ks) {
           if (!wait_fast(tok ? tfull_bar(stage) : full_bar(stage), phase, ctl)) { ok = false; break; }
           tc_fence_after();
+          if (tok) fence_proxy_async_shared();  // token scales were written by cp.async
           const int natoms = min(4, kc4 - 4 * ks);
           const uint32_t col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage + (tok ? 16 : 0));
           const uint64_t src = desc_scales(tok ? sSFB + stage * kSfStageBytes : sW + stage * kWStageBytes + kATileBytes);
@@ -677,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             break;
           }
           tc_fence_after();
+          fence_proxy_async_shared();  // the token rows were written by cp.async
           const int natoms = min(4, un.kc4 - 4 * ks);
           const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
           // K step a (32 bytes along the 128-byte swizzled rows): +2 in the address field
@@ -819,48 +825,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2-D byte tensor [rows, row_bytes] read in 128-byte x box_rows boxes with
-// the 128-byte swizzle (zero fill out of bounds).
-bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)kStageKBytes, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
                                 const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
                                 cudaStream_t s) {
   if (front && (early || front->S > kSmallSlots || front->S < 1)) return cudaErrorInvalidValue;
-  CUtensorMap tmB0, tmB1;
-  if (!make_map(&tmB0, j0.a_packed, (uint64_t)j0.K / 2, (uint64_t)R_max, kBBoxRows)) return cudaErrorInvalidValue;
-  if (j1 && !make_map(&tmB1, j1->a_packed, (uint64_t)j1->K / 2, (uint64_t)R_max, kBBoxRows))
-    return cudaErrorInvalidValue;
-  if (!j1) tmB1 = tmB0;
   if (j1 && !gate) return cudaErrorInvalidValue;
   GemmArgs p = {};
   auto fill = [](Job& J, const GemmJob& src) {
     J.w_tiled = src.w_tiled;
+    J.a_packed = src.a_packed;
     J.a_sf = src.a_sf;
     J.d = src.d;
     J.N = src.N;
@@ -899,7 +874,7 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
   const long long units_bound = chunks_bound(R_max, E) * (j0.N / kBM + (j1 ? j1->N / kBM : 0));
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
-  return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, tmB0, tmB1, p);
+  return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, p);
 }
 
 }  // namespace moe
