@@ -458,6 +458,28 @@ def test_layer_determinism_and_batch_invariance(small):
         assert torch.equal(yt[0].view(torch.int16), y0[t].view(torch.int16)), t
 
 
+@pytest.mark.parametrize("T,k,seed", [(1, 8, 0), (4, 8, 1), (32, 1, 2), (1, 32, 3), (3, 5, 4), (16, 2, 5)])
+def test_decode_layer_equals_stages(small, T, k, seed):
+    """Decode batches (T*k <= 32: the one-launch front end, in-kernel routing
+    in the GEMM launch) give the separate entry points' bits for any routing:
+    repeated experts in a token, unused slots, tokens with no rows, one slot
+    per token or 32 for one."""
+    E, _, _, _, W, *_ = small
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(100 + seed)
+    ids = torch.randint(-1, E, (T, k), generator=g, dtype=torch.int32)
+    if T > 1:
+        ids[T - 1] = -1                  # a token with no rows
+    tw = torch.rand((T, k), generator=g)
+    x = (torch.randn((T, W.H), generator=g)).to(torch.bfloat16)
+    x, ids, tw = x.to(dev), ids.to(dev), tw.to(dev)
+    y = torch.full((T, W.H), 3.0, dtype=torch.bfloat16, device=dev)
+    N.MoeLayer(W, T, k)(x, ids, tw, y)
+    st = run_stages(x, ids, tw, W, E)
+    assert torch.equal(y.view(torch.int16), st["y"].view(torch.int16))
+    assert N.check_status() == 0
+
+
 def test_graph_replay_matches_direct_call(small):
     """The layer step captured as a CUDA graph (PDL edges included) gives the
     same bits as the direct call, before and after its inputs are refilled."""
