@@ -263,8 +263,17 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
   const int blk = blockIdx.x;
-  if (blk >= routed_blocks(g, layout)) return;
-  const RowBlock rb = resolve_block(g, layout, blk);
+  RowBlock rb;
+  if (layout == MOE_SF_CHUNK32) {
+    // the block count and this block's table entry in flight together (the
+    // entry is in bounds whether or not the block is routed)
+    const int4 c = ld_cg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
+    if (blk >= routed_blocks(g, layout)) return;
+    rb = RowBlock{c.x, c.y, c.z};
+  } else {
+    if (blk >= routed_blocks(g, layout)) return;
+    rb = resolve_block(g, layout, blk);
+  }
   const int Kc = K / 16;
   const int kc0 = blockIdx.y * kColsPerCta;
   const int kcount = min(kColsPerCta, K - kc0);
@@ -272,23 +281,40 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   const int total = rb.nvalid * quads;
   const int lane = threadIdx.x & 31;
   const ScaleTarget st{sf + (size_t)blk * 128 * Kc, layout, Kc};  // either layout: 128*Kc bytes per block
-  for (int base = (threadIdx.x & ~31); base < total; base += blockDim.x) {
-    const int item = base + lane;
-    const bool active = item < total;
-    const int m = active ? item / quads : 0;
-    const int q = active ? item - m * quads : 0;
-    const int r = rb.row0 + m;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
-      const int srow = src_k > 0 ? ld_cg(g.row_slot + r) / src_k : r;
-      const uint2 u = ld_cg(reinterpret_cast<const uint2*>(src + (size_t)srow * K + kc0 + 4 * q));
-      v[0] = bf16_to_f32(u.x & 0xFFFFu);
-      v[1] = bf16_to_f32(u.x >> 16);
-      v[2] = bf16_to_f32(u.y & 0xFFFFu);
-      v[3] = bf16_to_f32(u.y >> 16);
+  // source row of each of the block's rows, read once
+  __shared__ int s_src[kRowsAtom];
+  if ((int)threadIdx.x < rb.nvalid) {
+    const int r = rb.row0 + threadIdx.x;
+    s_src[threadIdx.x] = src_k > 0 ? ld_cg(g.row_slot + r) / src_k : r;
+  }
+  __syncthreads();
+  // Up to kBatch of this warp's items loaded before any is quantized, so that
+  // a block of many rows costs one memory round trip per kBatch, not per row.
+  constexpr int kBatch = 8;
+  for (int base0 = (threadIdx.x & ~31); base0 < total; base0 += kBatch * blockDim.x) {
+    uint2 u[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int item = base0 + j * blockDim.x + lane;
+      u[j] = make_uint2(0u, 0u);
+      if (item < total) {
+        const int m = item / quads, q = item - m * quads;
+        u[j] = ld_cg(reinterpret_cast<const uint2*>(src + (size_t)s_src[m] * K + kc0 + 4 * q));
+      }
     }
-    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2,
-                        st.word(m, (kc0 + 4 * q) / 16));
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int base = base0 + j * blockDim.x;  // the same for the whole warp
+      if (base >= total) break;
+      const int item = base + lane;
+      const bool active = item < total;
+      const int m = active ? item / quads : 0;
+      const int q = active ? item - m * quads : 0;
+      const float v[4] = {bf16_to_f32(u[j].x & 0xFFFFu), bf16_to_f32(u[j].x >> 16), bf16_to_f32(u[j].y & 0xFFFFu),
+                          bf16_to_f32(u[j].y >> 16)};
+      quantize_quad_store(v, active, lane, packed + (size_t)(rb.row0 + m) * (K / 2) + (kc0 + 4 * q) / 2,
+                          st.word(m, (kc0 + 4 * q) / 16));
+    }
   }
   st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
 }
