@@ -282,21 +282,37 @@ def gpu_bench(args, rank, world):
         return {n: statistics.mean(v) for n, v in acc.items()}, statistics.mean(gemm_bytes)
 
     def time_e2e(c, items, steps):
-        """Through the public call with host buffers: pinned H2D of x, ids and
-        router weights into the layer's input buffers, the layer step (its
+        """Through the public call with host buffers: one pinned H2D copy of the
+        step's inputs (x, ids and router weights packed in one staging buffer,
+        whose device twin the layer reads in place), the layer step (its
         captured graph), D2H of y; all inside the timed region."""
         T_max = max(it["T"] for it in items)
         layer = N.MoeLayer(W, T_max, c.k)
+
+        def carve(buf, it):
+            # x | ids | tw, each section 256-byte aligned
+            T, k = it["T"], c.k
+            nx, ni = T * c.H * 2, T * k * 4
+            ox, oi, ow = 0, (nx + 255) // 256 * 256, 0
+            ow = oi + (ni + 255) // 256 * 256
+            x = buf[ox:ox + nx].view(torch.bfloat16).view(T, c.H)
+            ids = buf[oi:oi + ni].view(torch.int32).view(T, k)
+            tw = buf[ow:ow + ni].view(torch.float32).view(T, k)
+            return x, ids, tw, ow + ni
+
         host, dev_bufs, graphs = [], [], []
         for it in items:
-            host.append(dict(x=it["x"].cpu().pin_memory(), ids=it["ids_h"].pin_memory(),
-                             tw=it["tw_h"].pin_memory(), y=torch.empty_like(it["x"], device="cpu").pin_memory(),
-                             T=it["T"], G=it["G"]))
-            d = dict(x=torch.empty_like(it["x"]), ids=torch.empty_like(it["ids"]), tw=torch.empty_like(it["tw"]),
-                     y=torch.empty_like(it["x"]))
-            d["x"].copy_(it["x"]), d["ids"].copy_(it["ids"]), d["tw"].copy_(it["tw"])
-            graphs.append(layer.capture(d["x"], d["ids"], d["tw"], d["y"]))
-            dev_bufs.append(d)
+            size = carve(torch.empty(1 << 30, dtype=torch.uint8, device="meta"), it)[3]
+            hbuf = torch.empty(size, dtype=torch.uint8).pin_memory()
+            hx, hi, hw, _ = carve(hbuf, it)
+            hx.copy_(it["x"].cpu()), hi.copy_(it["ids_h"]), hw.copy_(it["tw_h"])
+            host.append(dict(buf=hbuf, y=torch.empty_like(it["x"], device="cpu").pin_memory(), T=it["T"], G=it["G"]))
+            dbuf = torch.empty(size, dtype=torch.uint8, device=dev)
+            dx, di, dw, _ = carve(dbuf, it)
+            dbuf.copy_(hbuf)
+            y = torch.empty_like(it["x"])
+            graphs.append(layer.capture(dx, di, dw, y))
+            dev_bufs.append(dict(buf=dbuf, y=y))
         ms, h2d, d2h, byts = [], [], [], []
         for i in range(steps + 3):
             h, d = host[i % len(host)], dev_bufs[i % len(host)]
@@ -304,16 +320,14 @@ def gpu_bench(args, rank, world):
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            d["x"].copy_(h["x"], non_blocking=True)
-            d["ids"].copy_(h["ids"], non_blocking=True)
-            d["tw"].copy_(h["tw"], non_blocking=True)
+            d["buf"].copy_(h["buf"], non_blocking=True)
             graphs[i % len(host)].replay()
             h["y"].copy_(d["y"], non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
             if i >= 3:
                 ms.append(e0.elapsed_time(e1))
-                h2d.append(d["x"].numel() * 2 + d["ids"].numel() * 4 + d["tw"].numel() * 4)
+                h2d.append(d["buf"].numel())
                 d2h.append(d["y"].numel() * 2)
                 byts.append(step_bytes(c, h["G"], h["T"]))
         return ms, byts, statistics.mean(h2d), statistics.mean(d2h)
