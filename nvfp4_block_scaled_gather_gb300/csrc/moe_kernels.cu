@@ -198,7 +198,7 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
 // Token-scale layouts (include/moe_nvfp4.h): per group 128-row atoms, or per
 // 32-row GEMM chunk one 512-byte atom per 64 K values whose 16-byte row i
 // holds chunk row i's four scales in its first word (other words zero).
-constexpr int kRowsAtom = 128, kRowsChunk = 32;
+constexpr int kRowsAtom = 128;
 
 struct ScaleTarget {
   uint8_t* base;  // the CTA's row block region

@@ -339,3 +339,41 @@ def moe_layer(x_bits, topk_ids, topk_w, weights: dict, E: int) -> dict:
     y = scatter_add(d2, row_slot, topk_ids, topk_w, weights["g_down"], T, E)
     return dict(row_slot=row_slot, group_offsets=offs, group_expert=gexp, xg=xg, xq=xq,
                 xsf=xsf, d13=d13, h=h, hq=hq, hsf=hsf, d2=d2, y=y)
+
+
+# ---------------------------------------------------------------------------
+# The GEMV path (W4A16): [P1] "Grouped vs GEMV at M=1" -- the pages keep it
+# as an explicit override and fallback; it multiplies the exact bf16
+# activations against the NVFP4 weights (no activation quantization), which is
+# why its output differs materially from the W4A4 grouped path's.
+# ---------------------------------------------------------------------------
+
+def grouped_gemv_w4a16(a_bits, group_offsets, group_expert, w_packed, w_sf_linear) -> np.ndarray:
+    """D[r, n] = sum_k a[r, k] * W_e[n, k] per group, with a[r, k] the exact
+    value of the bf16 activation and W the dequantized NVFP4 weight without its
+    global. Products of bf16 and e2m1*e4m3 values are exact in fp64."""
+    A = bf16_bits_to_f64(np.asarray(a_bits, dtype=np.uint16))
+    N = w_packed.shape[1]
+    D = np.zeros((A.shape[0], N), dtype=np.float64)
+    offs = np.asarray(group_offsets, dtype=np.int64)
+    for g, e in enumerate(np.asarray(group_expert, dtype=np.int64)):
+        r0, r1 = int(offs[g]), int(offs[g + 1])
+        Wg = dequantize_weight(w_packed[e], w_sf_linear[e])  # [N, K]
+        D[r0:r1] = A[r0:r1] @ Wg.T
+    return D
+
+
+def moe_layer_w4a16(x_bits, topk_ids, topk_w, weights: dict, E: int) -> dict:
+    """The routed-expert step on the GEMV path: the same route, SwiGLU (h
+    rounded once to bf16) and scatter-add as moe_layer, with both GEMMs taking
+    bf16 activations as they are instead of their NVFP4 quantization."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    topk_ids = np.asarray(topk_ids)
+    T, k = topk_ids.shape
+    row_slot, offs, gexp = route_groups(topk_ids, E)
+    xg = gather_rows(x_bits, row_slot, k)
+    d13 = grouped_gemv_w4a16(xg, offs, gexp, weights["w13_packed"], weights["w13_sf_linear"])
+    h = swiglu(d13, offs, gexp, weights["g_gate_up"])
+    d2 = grouped_gemv_w4a16(h, offs, gexp, weights["w2_packed"], weights["w2_sf_linear"])
+    y = scatter_add(d2, row_slot, topk_ids, topk_w, weights["g_down"], T, E)
+    return dict(row_slot=row_slot, group_offsets=offs, group_expert=gexp, xg=xg, d13=d13, h=h, d2=d2, y=y)

@@ -448,3 +448,75 @@ def check_unused_slots(O):
     y_masked = O.moe_layer(x, ids2, tw, wts, E=5)["y"]
     y_k1 = O.moe_layer(x, ids[:, :1], tw[:, :1], wts, E=5)["y"]
     assert np.array_equal(y_masked, y_k1)
+
+
+# ---------------------------------------------------------------------------
+# the GEMV path (W4A16): [P1] "Grouped vs GEMV at M=1"
+# ---------------------------------------------------------------------------
+
+def lossless_rows(rng, R, K):
+    """bf16 rows whose NVFP4 quantization loses nothing: each 16-block is a
+    power-of-two scale times e2m1 values, with one element at +-6 times it
+    (so the block scale is that power of two exactly)."""
+    vals = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    x = rng.choice(vals, size=(R, K)) * rng.choice([-1.0, 1.0], size=(R, K))
+    x[:, ::16] = 6.0 * rng.choice([-1.0, 1.0], size=(R, K // 16))
+    scale = np.exp2(rng.integers(-6, 4, size=(R, K // 16)).astype(np.float64)).repeat(16, axis=1)
+    return bf16_bits(x * scale)
+
+
+def check_gemv_w4a16_lossless(O):
+    """Where quantizing the activations loses nothing, W4A16 and W4A4 are the
+    same arithmetic: the GEMV path must equal the grouped GEMM exactly."""
+    rng = np.random.default_rng(31)
+    _, offs, gexp, w, wsf = tiny_gemm_case(seed=31)
+    x = lossless_rows(rng, int(offs[-1]), 64)
+    a, asf = O.quantize_rows(x, offs)
+    exact = torch.tensor(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.dequantize_rows(a, asf, offs), exact)  # the construction holds
+    assert np.array_equal(O.grouped_gemv_w4a16(x, offs, gexp, w, wsf), O.grouped_gemm(a, asf, offs, gexp, w, wsf))
+
+
+def check_gemv_w4a16_brute_force(O):
+    """Each output against the exact rational sum of bf16 activation times
+    e2m1 code times e4m3 scale (values read through torch, not the oracle)."""
+    x, offs, gexp, w, wsf = tiny_gemm_case(seed=37)
+    D = O.grouped_gemv_w4a16(x, offs, gexp, w, wsf)
+    xv = torch.tensor(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    e4m3_vals = torch_e4m3_values()
+    rng = np.random.default_rng(2)
+    for _ in range(24):
+        r = int(rng.integers(0, len(x)))
+        n = int(rng.integers(0, w.shape[1]))
+        e = gexp[int(np.searchsorted(offs, r, side="right") - 1)]
+        acc = Fraction(0)
+        for kk in range(x.shape[1]):
+            wn = (w[e, n, kk // 2] >> (4 * (kk % 2))) & 0xF
+            acc += (Fraction(float(xv[r, kk])) * Fraction(e2m1_value_from_bits(int(wn)))
+                    * Fraction(float(e4m3_vals[wsf[e, n, kk // 16]])))
+        assert abs(Fraction(float(D[r, n])) - acc) <= abs(acc) * Fraction(1, 2 ** 50), (r, n)
+
+
+def check_layer_w4a16(O):
+    """The GEMV-path step is batch invariant, and on losslessly quantizable
+    activations its first GEMM equals the grouped path's."""
+    x, ids, tw, wts = small_layer_inputs()
+    full = O.moe_layer_w4a16(x, ids, tw, wts, E=5)["y"]
+    for t in (0, 3, 5):
+        alone = O.moe_layer_w4a16(x[t:t + 1], ids[t:t + 1], tw[t:t + 1], wts, E=5)["y"]
+        assert np.array_equal(alone[0], full[t]), t
+    # the first GEMM of token 0's first slot, recomputed from the raw codes
+    res = O.moe_layer_w4a16(x, ids, tw, wts, E=5)
+    r = int(np.where(res["row_slot"] == 0)[0][0])
+    e = int(ids[0, 0])
+    xv = torch.tensor(x[0].view(np.int16)).view(torch.bfloat16).double().numpy()
+    e4m3_vals = torch_e4m3_values()
+    codes = np.stack([wts["w13_packed"][e] & 0xF, wts["w13_packed"][e] >> 4], axis=-1).reshape(len(wts["w13_packed"][e]), -1)
+    wv = np.vectorize(e2m1_value_from_bits)(codes) * np.repeat(e4m3_vals[wts["w13_sf_linear"][e]], 16, axis=1)
+    want = wv @ xv
+    assert np.allclose(res["d13"][r], want, rtol=1e-12, atol=0.0)
+    xl = lossless_rows(np.random.default_rng(41), x.shape[0], x.shape[1])
+    a = O.moe_layer_w4a16(xl, ids, tw, wts, E=5)
+    b = O.moe_layer(xl, ids, tw, wts, E=5)
+    assert np.array_equal(a["d13"], b["d13"])
+    assert np.array_equal(a["h"], b["h"])

@@ -13,7 +13,7 @@ PINS = [
     P.check_quantize_block_hand, P.check_pack_order, P.check_quantize_error_bound,
     P.check_grouping_brute, P.check_gather, P.check_gemm_brute_force, P.check_gemm_invariants,
     P.check_swiglu_closed_form, P.check_scatter_hand, P.check_layer_batch_invariance,
-    P.check_unused_slots,
+    P.check_unused_slots, P.check_gemv_w4a16_lossless, P.check_gemv_w4a16_brute_force, P.check_layer_w4a16,
 ]
 
 

@@ -30,6 +30,10 @@ MUTATIONS = {
     "rows visited backwards": ("for slot, e in enumerate(ids):", "for slot, e in reversed(list(enumerate(ids))):"),
     "groups in first-seen order": ("group_expert = sorted(rows_of)", "group_expert = list(rows_of)"),
     "gather by slot modulo": ("[np.asarray(row_slot) // k]", "[np.asarray(row_slot) % k]"),
+    "GEMV path rounds its activations": ("A = bf16_bits_to_f64(np.asarray(a_bits, dtype=np.uint16))",
+                                         "A = np.round(bf16_bits_to_f64(np.asarray(a_bits, dtype=np.uint16)) * 8) / 8"),
+    "GEMV path reads K backwards": ("D[r0:r1] = A[r0:r1] @ Wg.T", "D[r0:r1] = A[r0:r1] @ Wg[:, ::-1].T"),
+    "GEMV layer quantizes x": ("d13 = grouped_gemv_w4a16(xg, offs,", "d13 = grouped_gemv_w4a16(np.asarray(xg) & np.uint16(0xFFF0), offs,"),
     "zero block keeps codes": ("np.where((d == 0)[..., None], np.uint8(0), ", "np.where((d < 0)[..., None], np.uint8(0), "),
 }
 
