@@ -243,6 +243,27 @@ def gpu_bench(args, rank, world):
         byts = [step_bytes(c, items[i % len(items)]["G"], items[i % len(items)]["T"]) for i in range(steps)]
         return ms, byts
 
+    def time_w4a16(c, items, steps):
+        """The GEMV path (W4A16) of the same step, graph replays, L2 flushed
+        before each: a validation path, timed for the record."""
+        T_max = max(it["T"] for it in items)
+        layer = N.MoeLayerW4A16(W, T_max, c.k)
+        ys = [torch.empty_like(it["x"]) for it in items]
+        graphs = [layer.capture(it["x"], it["ids"], it["tw"], y) for it, y in zip(items, ys)]
+        for i in range(3):
+            graphs[i % len(items)].replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            graphs[i % len(items)].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        byts = [step_bytes(c, items[i % len(items)]["G"], items[i % len(items)]["T"]) for i in range(steps)]
+        return ms, byts
+
     def time_stages(c, items, steps):
         """Same kernels as the fused entry, launched stage by stage with
         events between them (per-kernel device time)."""
@@ -370,6 +391,13 @@ def gpu_bench(args, rank, world):
                                 "roof_frac": round(g2 / peak, 4),
                                 "mean_active_experts": statistics.mean(i["G"] for i in it2),
                                 "rows": statistics.mean(i["R"] for i in it2)}
+    # the GEMV path (W4A16, exact bf16 activations): a validation path, timed on the same workload
+    w4a16 = None
+    if world == 1 and not args.no_extra:
+        m3, b3 = time_w4a16(cfg, items, max(10, min(args.steps, 40)))
+        g3 = sum(b3) / (sum(m3) * 1e-3) / 1e9
+        w4a16 = {"workload": cfg.name, "ms_per_step": round(statistics.mean(m3), 5), "weight_gbs": round(g3, 1),
+                 "roof_frac": round(g3 / peak, 4), "launches_per_step": 5}
     # route, gather+quantize (one launch when T*k <= 32), the w13+w2 grouped GEMM (one
     # persistent launch), scatter
     launches_per_step = 3 if max(i["T"] for i in items) * cfg.k <= 32 else 4
@@ -418,6 +446,7 @@ def gpu_bench(args, rank, world):
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "per_config": per_config,
+        "w4a16_gemv_path": w4a16,
         "device": props.name,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

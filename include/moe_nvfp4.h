@@ -293,6 +293,35 @@ int moe_nvfp4_layer_static(const uint16_t* x, int T, int H, int I, const int32_t
                            const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
                            uint16_t* y, cudaStream_t stream);
 
+/* The GEMV path (W4A16). First page, the paragraph comparing the grouped and
+ * GEMV paths at M=1: the GEMV path multiplies the exact bf16 activations
+ * against the NVFP4 weights (no activation quantization), so its output
+ * differs materially from the W4A4 grouped path's; the page keeps it as an
+ * explicit override and fallback. Here it is the reference against which the
+ * grouped path's activation quantization is measured.
+ *
+ * nvfp4_grouped_gemv_w4a16 -- d[r, n] = sum_k a(r)[k] * W[e, n, k] for the
+ * rows r of each group (expert e), dequantized weight without its global,
+ * fp32 accumulation in a fixed K order (a row's result does not depend on the
+ * batch). Rows: a(r) = a[row_slot[r] / src_k] when src_k > 0 (gathered from
+ * the token rows [T, K], src_k = top-k), else a[r] ([R_max, K]); bf16,
+ * 16-byte aligned. w_tiled: nvfp4_tile_weights output for [E, N, K]
+ * (w_interleaved as there). d [R_max, N] fp32 (rows of routed slots written).
+ * N % 128 == 0, K % 64 == 0, K <= 14336; MOE_ERR_SHAPE otherwise. */
+int nvfp4_grouped_gemv_w4a16(const uint16_t* a, int src_k, const moe_groups_t* groups, int R_max,
+                             const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
+                             cudaStream_t stream);
+
+/* moe_nvfp4_layer_w4a16 -- the whole step a1..a8 on the GEMV path: route,
+ * w13 GEMV on the gathered bf16 rows, SwiGLU to bf16 h (no requantization),
+ * w2 GEMV on h, scatter-add; five launches. Arguments, weights and results as
+ * moe_nvfp4_layer; workspace of moe_nvfp4_layer_w4a16_workspace_size() bytes
+ * (256-byte aligned, any contents). H, I <= 14336. */
+size_t moe_nvfp4_layer_w4a16_workspace_size(int T, int k, int E, int H, int I);
+int moe_nvfp4_layer_w4a16(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
+                          const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
+                          void* workspace, size_t ws_bytes, uint16_t* y, cudaStream_t stream);
+
 /* Load-time helper (not part of the timed step): weight tiling for the
  * grouped GEMM. packed [rows, K/2] e2m1 and linear scales [rows, K/16] ->
  * `tiled` (nvfp4_tiled_bytes(rows, K) bytes): for each 128-row tile and each

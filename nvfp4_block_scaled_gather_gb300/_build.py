@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_nvfp4.so")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "nvfp4_gemm.cu", "moe_static.cu"]
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "nvfp4_gemm.cu", "nvfp4_gemv.cu", "moe_static.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -66,6 +66,11 @@ _SIGS = {
     "nvfp4_swizzle_block_scales": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
     "moe_nvfp4_layer_static": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                        ctypes.POINTER(MoeWeights), c_void_p, c_void_p]),
+    "nvfp4_grouped_gemv_w4a16": (c_int, [c_void_p, c_int, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int, c_int,
+                                         c_int, c_int, c_void_p, c_void_p]),
+    "moe_nvfp4_layer_w4a16_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "moe_nvfp4_layer_w4a16": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
+                                      ctypes.POINTER(MoeWeights), c_void_p, c_size_t, c_void_p, c_void_p]),
     "nvfp4_tiled_bytes": (c_size_t, [c_int, c_int]),
     "nvfp4_tile_weights": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
 }
@@ -300,6 +305,59 @@ def moe_nvfp4_layer(x, topk_ids, topk_w, weights: Weights, workspace, y, stream=
            load().moe_nvfp4_layer(_ptr(x), T, H, weights.I, _ptr(topk_ids), _ptr(topk_w), k,
                                   ctypes.byref(weights.struct), _ptr(workspace), workspace.numel(), _ptr(y),
                                   _stream(stream)))
+
+
+def nvfp4_grouped_gemv_w4a16(a, groups: Groups, w: TiledWeight, d, src_k: int = 0, R_max: int = None, stream=None):
+    """W4A16 grouped GEMV: bf16 rows a (gathered from token rows by slot when
+    src_k > 0, else row r = a[r]) times the tiled NVFP4 weight, fp32 d."""
+    K = a.shape[1]
+    assert K == w.K
+    if R_max is None:
+        R_max = a.shape[0] * (src_k if src_k > 0 else 1)
+    _check("nvfp4_grouped_gemv_w4a16",
+           load().nvfp4_grouped_gemv_w4a16(_ptr(a), src_k, ctypes.byref(groups.struct), R_max, _ptr(w.data),
+                                           int(w.interleaved), w.E, w.N, K, _ptr(d), _stream(stream)))
+
+
+def moe_nvfp4_layer_w4a16_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int:
+    return load().moe_nvfp4_layer_w4a16_workspace_size(T, k, E, H, I)
+
+
+def moe_nvfp4_layer_w4a16(x, topk_ids, topk_w, weights: Weights, workspace, y, stream=None):
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    _check("moe_nvfp4_layer_w4a16",
+           load().moe_nvfp4_layer_w4a16(_ptr(x), T, H, weights.I, _ptr(topk_ids), _ptr(topk_w), k,
+                                        ctypes.byref(weights.struct), _ptr(workspace), workspace.numel(), _ptr(y),
+                                        _stream(stream)))
+
+
+class MoeLayerW4A16:
+    """The GEMV path (W4A16) of the step, with its own workspace for up to T_max tokens."""
+
+    def __init__(self, weights: Weights, T_max: int, k: int):
+        import torch
+        self.weights, self.k, self.T_max = weights, k, T_max
+        n = moe_nvfp4_layer_w4a16_workspace_size(T_max, k, weights.E, weights.H, weights.I)
+        self.workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=weights.w13.data.device)
+
+    def __call__(self, x, topk_ids, topk_w, y=None, stream=None):
+        import torch
+        assert x.shape[0] <= self.T_max and topk_ids.shape[1] == self.k
+        if y is None:
+            y = torch.empty_like(x)
+        moe_nvfp4_layer_w4a16(x, topk_ids, topk_w, self.weights, self.workspace, y, stream)
+        return y
+
+    def capture(self, x, topk_ids, topk_w, y):
+        """One GEMV-path step on these device buffers as a CUDA graph."""
+        import torch
+        self(x, topk_ids, topk_w, y)  # one-time lookups outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            moe_nvfp4_layer_w4a16(x, topk_ids, topk_w, self.weights, self.workspace, y)
+        return graph
 
 
 STATIC_SCRATCH_BYTES = 8 << 20  # MOE_NVFP4_STATIC_SCRATCH_BYTES

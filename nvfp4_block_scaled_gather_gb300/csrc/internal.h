@@ -114,4 +114,11 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
                                 const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
                                 cudaStream_t s);
 
+// W4A16 grouped GEMV (nvfp4_gemv.cu): d [R_max, N] fp32 = bf16 rows times the
+// group's expert's tiled NVFP4 weight [E, N, K] (no global); rows are
+// a[row_slot[r] / src_k] (src_k > 0) or a[r]. N % 128 == 0, K % 64 == 0,
+// K <= 14336 (four rows of fp32 activations staged in shared memory).
+cudaError_t launch_gemv_w4a16(const uint16_t* a, int src_k, int R_max, int E, const moe_groups_t& g,
+                              const uint8_t* w_tiled, bool interleaved, int N, int K, float* d, cudaStream_t s);
+
 }  // namespace moe

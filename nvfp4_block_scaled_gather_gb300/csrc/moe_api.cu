@@ -87,6 +87,35 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   return w;
 }
 
+// The GEMV path's workspace: group metadata, fp32 w13 output, bf16 h, fp32 w2 output.
+struct GemvWs {
+  moe_groups_t groups;
+  float* d13;
+  uint16_t* h;
+  float* d2;
+  size_t bytes;
+};
+
+GemvWs carve_layer_w4a16(void* base, int T, int k, int E, int H, int I) {
+  GemvWs w;
+  const size_t S = (size_t)T * k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  uint8_t* gmem = take(moe_groups_bytes(T, k, E));
+  if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
+  w.d13 = reinterpret_cast<float*>(take(S * 2 * I * sizeof(float)));
+  w.h = reinterpret_cast<uint16_t*>(take(S * I * sizeof(uint16_t)));
+  w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
+  w.bytes = off;
+  return w;
+}
+
+constexpr int kGemvMaxK = 14336;  // four fp32 activation rows of K in 227 KB of shared memory
+
 }  // namespace
 
 int num_sms() {
@@ -360,6 +389,53 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (err == cudaSuccess)
     err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, small ? &front : nullptr, !small, st,
                               stream);
+  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+  return status_of(err);
+}
+
+int nvfp4_grouped_gemv_w4a16(const uint16_t* a, int src_k, const moe_groups_t* groups, int R_max,
+                             const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
+                             cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0 || src_k < 0 || src_k > kMaxTopK)
+    return MOE_ERR_INVALID;
+  if (N % 128 || K % 64 || K > kGemvMaxK || (w_interleaved && N % 256)) return MOE_ERR_SHAPE;
+  if ((long long)E * N > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (R_max == 0) return MOE_OK;
+  if (!a || !w_tiled || !d) return MOE_ERR_INVALID;
+  if (misaligned(a) || misaligned(w_tiled) || misaligned(d)) return MOE_ERR_INVALID;
+  return status_of(launch_gemv_w4a16(a, src_k, R_max, E, *groups, w_tiled, w_interleaved != 0, N, K, d, stream));
+}
+
+size_t moe_nvfp4_layer_w4a16_workspace_size(int T, int k, int E, int H, int I) {
+  if (T < 0 || k < 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+  return carve_layer_w4a16(nullptr, T, k, E, H, I).bytes;
+}
+
+int moe_nvfp4_layer_w4a16(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w,
+                          int k, const moe_nvfp4_weights_t* w, void* workspace, size_t ws_bytes, uint16_t* y,
+                          cudaStream_t stream) {
+  if (!w || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
+    return MOE_ERR_INVALID;
+  if (H % 128 || I % 128 || H > kGemvMaxK || I > kGemvMaxK) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(y)) return MOE_ERR_INVALID;
+  if (!w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !w->g_down) return MOE_ERR_INVALID;
+  if (misaligned(w->w13_tiled) || misaligned(w->w2_tiled)) return MOE_ERR_INVALID;
+  if ((long long)T * k > (1LL << 30) || (long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
+  if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
+  const int E = w->E, S = T * k;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return MOE_ERR_INVALID;
+  const GemvWs ws = carve_layer_w4a16(workspace, T, k, E, H, I);
+  if (ws_bytes < ws.bytes) return MOE_ERR_WORKSPACE;
+  // a1 route; a2+a4 gather and w13 GEMV on the exact bf16 rows; a5 SwiGLU to
+  // bf16 h (no requantization); a7 w2 GEMV on h; a8 scatter-add
+  cudaError_t err = launch_route(topk_ids, S, E, ws.groups, stream);
+  if (err == cudaSuccess)
+    err = launch_gemv_w4a16(x, k, S, E, ws.groups, w->w13_tiled, true, 2 * I, H, ws.d13, stream);
+  if (err == cudaSuccess)
+    err = launch_swiglu(ws.d13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, ws.h, nullptr, nullptr, stream);
+  if (err == cudaSuccess) err = launch_gemv_w4a16(ws.h, 0, S, E, ws.groups, w->w2_tiled, false, H, I, ws.d2, stream);
   if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
   return status_of(err);
 }

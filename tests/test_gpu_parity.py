@@ -78,7 +78,7 @@ def check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, H, I):
 
 
 # ---------------------------------------------------------------------------
-# tiny config (BASELINE tiny layer: 8 experts, hidden 256, intermediate 128)
+# tiny config (8 experts, hidden 256, intermediate 128)
 # ---------------------------------------------------------------------------
 
 @pytest.fixture(scope="module")
