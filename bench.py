@@ -590,7 +590,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_m1")
-    ap.add_argument("--extra", default="decode_m8,decode_m32,full_stream,large_batch",
+    ap.add_argument("--extra", default="decode_m8,decode_m32,full_stream,large_batch,prefill_m32",
                     help="further configs timed on one GPU and reported under per_config")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--profile", action="store_true", help="short run for ncu: warm-up and timed steps only")

@@ -65,6 +65,9 @@ CONFIGS = {
     "large_batch": LayerConfig("large_batch", E=288, H=4096, I=2048, k=8, routing="all_experts",
                                mg_lo=1, mg_hi=15, router_weights="uniform"),
     "decode_m32": LayerConfig("decode_m32", E=288, H=4096, I=2048, k=8, routing="topk", T=32),
+    # prefill-sized: every expert Mg ~ U{16..48} rows (mean 32, ~9216 rows, ~1152 tokens)
+    "prefill_m32": LayerConfig("prefill_m32", E=288, H=4096, I=2048, k=8, routing="all_experts",
+                               mg_lo=16, mg_hi=48, router_weights="uniform"),
 }
 
 

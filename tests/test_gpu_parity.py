@@ -538,7 +538,8 @@ def _token_check(t, x_np, ids_np, tw_np, w_or, E, gpu_y, gpu_st=None):
 
 
 @pytest.mark.parametrize("name,tokens", [("decode_m1", (0,)), ("decode_m8", (0, 5)), ("decode_m32", (3, 31)),
-                                         ("full_stream", (0, 40)), ("large_batch", (1, 150, 287))])
+                                         ("full_stream", (0, 40)), ("large_batch", (1, 150, 287)),
+                                         ("prefill_m32", (0, 600, 1100))])
 def test_full_size_layer(cuda, full_weights, name, tokens):
     cfg = CONFIGS[name]
     w, W, w_or = full_weights
