@@ -360,8 +360,12 @@ def gpu_bench(args, rank, world):
     items = workload(cfg)
     if args.profile:
         # short run for profilers: warm-up, then the timed steps, nothing else
-        ms, byts = time_layer(cfg, items, args.steps, args.warmup, graph=False)
-        print(json.dumps({"profile_run": cfg.name, "experts": cfg.E, "ms_per_step": statistics.mean(ms)}))
+        if args.path == "w4a16":
+            ms, byts = time_w4a16(cfg, items, args.steps)
+        else:
+            ms, byts = time_layer(cfg, items, args.steps, args.warmup, graph=False)
+        print(json.dumps({"profile_run": cfg.name, "path": args.path, "experts": cfg.E,
+                          "ms_per_step": statistics.mean(ms)}))
         return
     sampler = ClockSampler(gpu_id)
     sampler.wait_first()
@@ -594,6 +598,8 @@ def main():
                     help="further configs timed on one GPU and reported under per_config")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--profile", action="store_true", help="short run for ncu: warm-up and timed steps only")
+    ap.add_argument("--path", default="w4a4", choices=["w4a4", "w4a16"],
+                    help="with --profile: the grouped path (w4a4) or the GEMV path (w4a16)")
     ap.add_argument("--eager", action="store_true", help="time direct calls instead of CUDA-graph replays")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
