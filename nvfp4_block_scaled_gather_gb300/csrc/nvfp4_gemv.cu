@@ -32,6 +32,7 @@ constexpr int kGemvThreads = 256;
 constexpr int kRowsPass = 4;          // activation rows staged per pass
 constexpr int kStageBytes = 18432;    // one tiled K stage: 16 KB of codes, 2 KB of scale atoms
 constexpr int kCodeBytes = 16384;
+constexpr int kMaxK = 14336;          // kRowsPass fp32 rows of K in 224 KB of shared memory
 
 // Eight e2m1 codes (element 2j in the low nibble of byte j) -> four f16x2,
 // element 2j in the low half.
@@ -168,9 +169,12 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_w4a16_kernel(const uint16_t
 
 cudaError_t launch_gemv_w4a16(const uint16_t* a, int src_k, int R_max, int E, const moe_groups_t& g,
                               const uint8_t* w_tiled, bool interleaved, int N, int K, float* d, cudaStream_t s) {
-  if (N % 128 || K % 64 || K <= 0 || (interleaved && N % 256)) return cudaErrorInvalidValue;
+  if (N % 128 || K % 64 || K <= 0 || K > kMaxK || (interleaved && N % 256)) return cudaErrorInvalidValue;
   const int smem = kRowsPass * K * (int)sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(gemv_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // One fixed limit for every launch: lowering it for a smaller K would leave
+  // an already captured larger launch (a graph node of the w13 GEMV) above it.
+  cudaError_t err = cudaFuncSetAttribute(gemv_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRowsPass * kMaxK * (int)sizeof(float));
   if (err != cudaSuccess) return err;
   const int groups = R_max < E ? R_max : E;
   if (groups <= 0) return cudaSuccess;
