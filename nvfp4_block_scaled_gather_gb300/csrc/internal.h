@@ -60,8 +60,12 @@ cudaError_t launch_swiglu(const float* d13, int R_max, int E, int I, const moe_g
 cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int rows, int K, int interleave_rows,
                         uint8_t* tiled, cudaStream_t s);
 inline size_t tiled_bytes(long long rows, long long K) { return (size_t)(rows / 128) * ((K + 255) / 256) * 18432; }
+// tables_early: the routing tables (and topk_ids, topk_w, g_down) were written
+// two or more launches back, so they are read before waiting for the previous
+// kernel (which must have waited for its own predecessor before it triggered).
 cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k,
-                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s);
+                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s,
+                           bool tables_early = false);
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s);
 
 // tcgen05 grouped GEMM (nvfp4_gemm.cu), one persistent launch over one or

@@ -389,7 +389,8 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (err == cudaSuccess)
     err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, small ? &front : nullptr, !small, st,
                               stream);
-  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+  if (err == cudaSuccess)  // its routing tables are two or more launches old
+    err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream, true);
   return status_of(err);
 }
 
@@ -436,7 +437,8 @@ int moe_nvfp4_layer_w4a16(const uint16_t* x, int T, int H, int I, const int32_t*
   if (err == cudaSuccess)
     err = launch_swiglu(ws.d13, S, E, I, ws.groups, MOE_SF_CHUNK32, w->g_gate_up, ws.h, nullptr, nullptr, stream);
   if (err == cudaSuccess) err = launch_gemv_w4a16(ws.h, 0, S, E, ws.groups, w->w2_tiled, false, H, I, ws.d2, stream);
-  if (err == cudaSuccess) err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream);
+  if (err == cudaSuccess)  // its routing tables are two or more launches old
+    err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream, true);
   return status_of(err);
 }
 

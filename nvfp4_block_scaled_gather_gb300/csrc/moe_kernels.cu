@@ -487,9 +487,14 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
                                                            const int32_t* __restrict__ ids,
                                                            const float* __restrict__ topk_w, int k, int E,
                                                            moe_groups_t g, const float* __restrict__ g_down,
-                                                           uint16_t* __restrict__ y) {
-  pdl_wait();  // the previous kernel in the stream may still be running
-  pdl_trigger();
+                                                           uint16_t* __restrict__ y, int tables_early) {
+  // The previous kernel in the stream may still be running. With
+  // tables_early the routing tables are two or more launches old (complete):
+  // only the reads of d2 wait for it.
+  if (!tables_early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_coef[kMaxTopK];
   __shared__ int s_n;
@@ -513,6 +518,10 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
     if (lane == 0) s_n = __popc(valid);
   }
   __syncthreads();
+  if (tables_early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int col = blockIdx.y * (kThreads * 4) + threadIdx.x * 4;
   if (col >= H) return;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -651,9 +660,11 @@ cudaError_t launch_tile(const uint8_t* packed, const uint8_t* sf_linear, int row
 }
 
 cudaError_t launch_scatter(const float* d2, int H, const int32_t* topk_ids, const float* topk_w, int T, int k,
-                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s) {
+                           int E, const moe_groups_t& g, const float* g_down, uint16_t* y, cudaStream_t s,
+                           bool tables_early) {
   dim3 grid(T, (H + kThreads * 4 - 1) / (kThreads * 4));
-  return launch_pdl(scatter_kernel, grid, dim3(kThreads), 0, s, d2, H, topk_ids, topk_w, k, E, g, g_down, y);
+  return launch_pdl(scatter_kernel, grid, dim3(kThreads), 0, s, d2, H, topk_ids, topk_w, k, E, g, g_down, y,
+                    tables_early ? 1 : 0);
 }
 
 cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzled, cudaStream_t s) {
