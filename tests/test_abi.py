@@ -23,7 +23,8 @@ def test_header_declares_the_hot_path():
     names = set(declared_functions())
     for n in ("moe_gather_rows", "nvfp4_quantize_rows", "nvfp4_grouped_gemm", "swiglu_grouped",
               "moe_scatter_add", "moe_nvfp4_layer", "moe_nvfp4_layer_workspace_size",
-              "nvfp4_swizzle_block_scales", "moe_route_groups"):
+              "nvfp4_swizzle_block_scales", "moe_route_groups", "nvfp4_grouped_gemv_w4a16",
+              "moe_nvfp4_layer_w4a16", "moe_nvfp4_layer_w4a16_workspace_size"):
         assert n in names, n
 
 
@@ -80,7 +81,22 @@ def test_host_side_validation(native):
     ws = native.moe_nvfp4_layer_workspace_size(4, 2, 8, 256, 128)
     assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 256, ws - 1, 16, s) == 5
     assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 300, ws, 16, s) == 1
+    # the GEMV path: shapes (N % 128, K % 64, K <= 14336, interleaved N % 256), alignment, src_k
+    assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 0, 4, 100, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 0, 4, 128, 96, 16, s) == 2
+    assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 0, 4, 128, 14400, 16, s) == 2
+    assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 1, 4, 384, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemv_w4a16(24, 2, ctypes.byref(g), 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemv_w4a16(16, -1, ctypes.byref(g), 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemv_w4a16(16, 2, None, 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.moe_nvfp4_layer_w4a16(16, 4, 200, 128, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
+    assert native.moe_nvfp4_layer_w4a16(16, 4, 16384, 128, 16, 16, 2, ctypes.byref(w), 256, 1 << 20, 16, s) == 2
+    ws16 = native.moe_nvfp4_layer_w4a16_workspace_size(4, 2, 8, 256, 128)
+    assert ws16 > 0
+    assert native.moe_nvfp4_layer_w4a16(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 256, ws16 - 1, 16, s) == 5
+    assert native.moe_nvfp4_layer_w4a16(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 300, ws16, 16, s) == 1
     # empty problems are no-ops
+    assert native.moe_nvfp4_layer_w4a16(None, 0, 256, 128, None, None, 2, ctypes.byref(w), None, 0, None, s) == 0
     assert native.moe_nvfp4_layer(None, 0, 256, 128, None, None, 2, ctypes.byref(w), None, 0, None, s) == 0
     assert native.nvfp4_swizzle_block_scales(None, 0, 64, None, s) == 0
 
