@@ -293,8 +293,8 @@ int moe_nvfp4_layer_static(const uint16_t* x, int T, int H, int I, const int32_t
                            const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,
                            uint16_t* y, cudaStream_t stream);
 
-/* The GEMV path (W4A16). First page, the paragraph comparing the grouped and
- * GEMV paths at M=1: the GEMV path multiplies the exact bf16 activations
+/* The GEMV path (W4A16). First page, section "Proof", the paragraph comparing
+ * the grouped and GEMV paths at M=1: the GEMV path multiplies the exact bf16 activations
  * against the NVFP4 weights (no activation quantization), so its output
  * differs materially from the W4A4 grouped path's; the page keeps it as an
  * explicit override and fallback. Here it is the reference against which the

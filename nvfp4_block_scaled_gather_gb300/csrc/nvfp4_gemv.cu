@@ -1,9 +1,10 @@
 // W4A16 grouped GEMV: the exact bf16 activations of each group's rows against
 // the group's expert's NVFP4 weight, no activation quantization. This is the
 // GEMV path of the rocket blog page "The CUTLASS grouped GEMM beats the scalar
-// GEMV loop at every M" (the paragraph comparing the two paths at M=1): kept
-// there as an explicit override and fallback, and the reference for how far
-// the W4A4 path's activation quantization moves the result.
+// GEMV loop at every M" (section "Proof", its paragraph comparing the two
+// paths at M=1): kept there as an explicit override and fallback, and the
+// reference for how far the W4A4 path's activation quantization moves the
+// result.
 //
 //   d[r, n] = sum_k a[r, k] * W[e, n, k]      (dequantized weight, no global)
 //

@@ -342,7 +342,7 @@ def moe_layer(x_bits, topk_ids, topk_w, weights: dict, E: int) -> dict:
 
 
 # ---------------------------------------------------------------------------
-# The GEMV path (W4A16): [P1] "Grouped vs GEMV at M=1" -- the pages keep it
+# The GEMV path (W4A16): [P1] "Proof" (grouped vs GEMV at M=1) -- the pages keep it
 # as an explicit override and fallback; it multiplies the exact bf16
 # activations against the NVFP4 weights (no activation quantization), which is
 # why its output differs materially from the W4A4 grouped path's.

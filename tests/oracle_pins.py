@@ -451,7 +451,7 @@ def check_unused_slots(O):
 
 
 # ---------------------------------------------------------------------------
-# the GEMV path (W4A16): [P1] "Grouped vs GEMV at M=1"
+# the GEMV path (W4A16): [P1] "Proof" (grouped vs GEMV at M=1)
 # ---------------------------------------------------------------------------
 
 def lossless_rows(rng, R, K):
