@@ -124,7 +124,9 @@ const char* moe_nvfp4_error_string(int status);
 /* Reads and clears the device-side status word of the current device after
  * synchronizing `stream`: MOE_OK, or MOE_ERR_TIMEOUT if a kernel's bounded
  * wait gave up since the last check (its outputs are then invalid). Returns
- * MOE_ERR_CUDA if the synchronization itself fails. */
+ * MOE_ERR_CUDA if the synchronization itself fails. The word's device address
+ * is looked up on a device's first call and kept for the life of the process:
+ * it is not valid after the device's context is reset (cudaDeviceReset). */
 int moe_nvfp4_check_status(cudaStream_t stream);
 
 /* Bytes of the group metadata for T tokens, top-k, E experts; and a carve of
@@ -280,11 +282,15 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
  * MOE_NVFP4_STATIC_SCRATCH_BYTES (8 MiB), held by every GPU that loads the
  * library until the process exits. Sizes whose
  * moe_nvfp4_layer_workspace_size() exceeds it return MOE_ERR_WORKSPACE (at
- * H = 4096, I = 2048, E = 288 that allows T*k <= 64, i.e. decode up to 8
- * streams of top-8). Nothing is allocated: the first call on a device looks up
- * the array's device address once (make that first call before any stream
- * capture); no part of the array needs to start at zero, every byte the step
- * reads is written earlier in the same call. All calls share the one array:
+ * H = 4096, I = 2048, E = 288 that allows T*k <= 119, i.e. decode up to 14
+ * streams of top-8); arguments are checked as by moe_nvfp4_layer first, with
+ * the same status codes. Nothing is allocated: the first call on a device
+ * looks up the array's device address once and keeps it for the life of the
+ * process (make that first call before any stream capture; the address is
+ * not valid after the device's context is reset with cudaDeviceReset, and
+ * calls after such a reset are not supported); no part of the array needs to
+ * start at zero, every byte the step reads is written earlier in the same
+ * call. All calls share the one array:
  * calls that can overlap on the GPU (different streams, or the same stream
  * from several host threads without ordering) race and must be serialized by
  * the caller. Arguments and results otherwise as moe_nvfp4_layer. */

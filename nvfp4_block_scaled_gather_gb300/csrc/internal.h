@@ -35,6 +35,11 @@ inline size_t token_sf_bytes(long long R_max, long long G_max, long long K, int 
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// Host-side argument checks of moe_nvfp4_layer (everything but the
+// workspace): MOE_OK, MOE_ERR_INVALID or MOE_ERR_SHAPE. T == 0 is valid.
+int layer_arg_status(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w, int k,
+                     const moe_nvfp4_weights_t* w, const uint16_t* y);
+
 // zero/nzero: an int array the route kernel also clears (may be null).
 cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s,
                          int* zero = nullptr, int nzero = 0);

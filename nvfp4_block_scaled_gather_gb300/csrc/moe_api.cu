@@ -118,6 +118,20 @@ constexpr int kGemvMaxK = 14336;  // four fp32 activation rows of K in 227 KB of
 
 }  // namespace
 
+int layer_arg_status(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w, int k,
+                     const moe_nvfp4_weights_t* w, const uint16_t* y) {
+  if (!w || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
+    return MOE_ERR_INVALID;
+  if (H % 128 || I % 128) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
+  if (misaligned(x) || misaligned(y)) return MOE_ERR_INVALID;
+  if (!w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !w->g_down) return MOE_ERR_INVALID;
+  if (misaligned(w->w13_tiled) || misaligned(w->w2_tiled)) return MOE_ERR_INVALID;
+  if ((long long)T * k > (1LL << 30) || (long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
 int num_sms() {
   const int dev = current_device();
   if (dev < 0) return 148;
@@ -349,16 +363,9 @@ size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I) {
 int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w, int k,
                     const moe_nvfp4_weights_t* w, void* workspace, size_t ws_bytes, uint16_t* y,
                     cudaStream_t stream) {
-  if (!w || T < 0 || k < 0 || k > kMaxTopK || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
-    return MOE_ERR_INVALID;
-  if (H % 128 || I % 128) return MOE_ERR_SHAPE;
+  const int arg_status = layer_arg_status(x, T, H, I, topk_ids, topk_w, k, w, y);
+  if (arg_status != MOE_OK) return arg_status;
   if (T == 0) return MOE_OK;
-  if (!x || !y || (k > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID;
-  if (misaligned(x) || misaligned(y)) return MOE_ERR_INVALID;
-  if (!w->w13_tiled || !w->g_gate_up || !w->w2_tiled || !w->g_down) return MOE_ERR_INVALID;
-  if (reinterpret_cast<uintptr_t>(w->w13_tiled) % 16 || reinterpret_cast<uintptr_t>(w->w2_tiled) % 16)
-    return MOE_ERR_INVALID;
-  if ((long long)T * k > (1LL << 30) || (long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
   if (k == 0) return status_of(cudaMemsetAsync(y, 0, (size_t)T * H * sizeof(uint16_t), stream));
   const int E = w->E;
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return MOE_ERR_INVALID;

@@ -47,9 +47,11 @@ void* scratch_address(int* status) {
 extern "C" int moe_nvfp4_layer_static(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
                                       const float* topk_w, int k, const moe_nvfp4_weights_t* w, uint16_t* y,
                                       cudaStream_t stream) {
-  if (!w || T < 0 || k < 0 || H <= 0 || I <= 0 || w->E <= 0) return MOE_ERR_INVALID;
-  const size_t need = moe_nvfp4_layer_workspace_size(T, k, w->E, H, I);
-  if (need > (size_t)MOE_NVFP4_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  // the same argument checks (and status codes) as moe_nvfp4_layer, before the size limit
+  const int arg_status = moe::layer_arg_status(x, T, H, I, topk_ids, topk_w, k, w, y);
+  if (arg_status != MOE_OK) return arg_status;
+  if (T > 0 && k > 0 && moe_nvfp4_layer_workspace_size(T, k, w->E, H, I) > (size_t)MOE_NVFP4_STATIC_SCRATCH_BYTES)
+    return MOE_ERR_WORKSPACE;
   int status = MOE_OK;
   void* scratch = moe::scratch_address(&status);
   if (status != MOE_OK) return status;

@@ -100,6 +100,28 @@ def make_weights(E: int, H: int, I: int, seed: int = SEED_WEIGHTS, device="cpu")
                 w2_packed=w2, w2_sf_linear=w2_sf, g_down=g_down)
 
 
+def make_edge_weights(E: int, H: int, I: int, seed: int = SEED_WEIGHTS, device="cpu") -> dict:
+    """Expert weights as make_weights, but with e4m3 block-scale codes drawn
+    uniformly over every finite non-negative code, 0x00 .. 0x7E: a zero scale
+    (the whole 16-value block is zero), the subnormals 0x01 .. 0x07
+    (m * 2^-9), the small normals and the largest value (448). The first
+    rocket blog page ("Proof") tests with constant and random per-block
+    scales; this draw puts every scale value the format has in front of the
+    GEMM. Codes only: no codec runs here."""
+    g = _gen(seed, device)
+    u8 = dict(dtype=torch.uint8, device=device, generator=g)
+    w13 = torch.randint(0, 256, (E, 2 * I, H // 2), **u8)
+    w13_sf = torch.randint(0, SCALE_CODE_HI + 1, (E, 2 * I, H // 16), **u8)
+    w2 = torch.randint(0, 256, (E, H, I // 2), **u8)
+    w2_sf = torch.randint(0, SCALE_CODE_HI + 1, (E, H, I // 16), **u8)
+    z = torch.randn((E, 2), dtype=torch.float32, device=device, generator=g)
+    g_gate = GATE_GLOBAL * torch.exp(0.05 * z[:, 0])
+    g_gate_up = torch.stack([g_gate, g_gate / GATE_UP_RATIO], dim=1).contiguous()
+    g_down = (DOWN_GLOBAL * torch.exp(0.05 * z[:, 1])).contiguous()
+    return dict(w13_packed=w13, w13_sf_linear=w13_sf, g_gate_up=g_gate_up,
+                w2_packed=w2, w2_sf_linear=w2_sf, g_down=g_down)
+
+
 def make_activations(T: int, H: int, seed: int = SEED_ACTIVATIONS, device="cpu") -> torch.Tensor:
     """x [T, H] bf16 drawn N(0, 1)."""
     g = _gen(seed, device)

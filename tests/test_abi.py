@@ -81,6 +81,14 @@ def test_host_side_validation(native):
     ws = native.moe_nvfp4_layer_workspace_size(4, 2, 8, 256, 128)
     assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 256, ws - 1, 16, s) == 5
     assert native.moe_nvfp4_layer(16, 4, 256, 128, 16, 16, 2, ctypes.byref(w), 300, ws, 16, s) == 1
+    # the allocation-free entry checks its arguments like moe_nvfp4_layer, before its size limit:
+    # a batch far beyond the scratch array still gets the shape / argument error first
+    assert native.moe_nvfp4_layer_static(16, 4096, 200, 128, 16, 16, 8, ctypes.byref(w), 16, s) == 2
+    assert native.moe_nvfp4_layer_static(16, 4096, 256, 96, 16, 16, 8, ctypes.byref(w), 16, s) == 2
+    assert native.moe_nvfp4_layer_static(16, 4096, 256, 128, 16, 16, 33, ctypes.byref(w), 16, s) == 1
+    assert native.moe_nvfp4_layer_static(16, 4096, 256, 128, 16, 16, 8, None, 16, s) == 1
+    assert native.moe_nvfp4_layer_static(24, 4096, 256, 128, 16, 16, 8, ctypes.byref(w), 16, s) == 1
+    assert native.moe_nvfp4_layer_static(16, 4096, 256, 128, 16, 16, 8, ctypes.byref(w), 16, s) == 5
     # the GEMV path: shapes (N % 128, K % 64, K <= 14336, interleaved N % 256), alignment, src_k
     assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 0, 4, 100, 256, 16, s) == 2
     assert native.nvfp4_grouped_gemv_w4a16(16, 2, ctypes.byref(g), 8, 16, 0, 4, 128, 96, 16, s) == 2

@@ -17,64 +17,15 @@ from nvfp4_block_scaled_gather_gb300 import _native as N
 from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_layer, make_weights, make_activations, \
     make_routing
 from oracle import nvfp4_moe as O
-from tests.gpu_cases import (LazyExperts, bf16_to_np, bf16_ulps, chunk32_bytes, np_to_bf16, oracle_weights,
-                             rel_fro, row_scales, run_stages, small_case, weights_from)
+from tests.gpu_cases import (GEMM_TOL, LAYER_TOL, assert_swiglu_close, bf16_to_np, check_groups,
+                             check_stages_against_oracle, chunk32_bytes, chunk32_row_scales, edge_rows, np_to_bf16,
+                             oracle_weights, rel_fro, row_scales, run_stages, small_case, weights_from)
 
 pytestmark = pytest.mark.gpu
-
-GEMM_TOL = 1e-5
-LAYER_TOL = 1e-2
 
 
 def np_inputs(x, ids, tw):
     return bf16_to_np(x), ids.cpu().numpy(), tw.cpu().numpy()
-
-
-def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
-    G = len(ref_gexp)
-    assert host["G"] == G and host["R"] == len(ref_row_slot)
-    assert np.array_equal(host["group_expert"].numpy(), ref_gexp)
-    assert np.array_equal(host["group_offsets"].numpy(), ref_offs)
-    assert np.array_equal(host["row_slot"].numpy(), ref_row_slot)
-    assert np.array_equal(host["group_sf_block"].numpy(), O.group_sf_blocks(ref_offs))
-    chunks = np.concatenate([[0], np.cumsum((np.diff(ref_offs) + 31) // 32)])
-    assert np.array_equal(host["group_chunk"].numpy(), chunks) and host["chunks"] == chunks[-1]
-    info = [(ref_offs[g] + 32 * q, min(32, ref_offs[g + 1] - ref_offs[g] - 32 * q), ref_gexp[g], g)
-            for g in range(G) for q in range(chunks[g + 1] - chunks[g])]
-    assert np.array_equal(host["chunk_info"].numpy(), np.array(info, dtype=np.int64).reshape(-1, 4))
-    assert host["max_mg"] == (int(np.diff(ref_offs).max()) if G else 0)
-    slot_row = np.full(S, -1)
-    slot_row[ref_row_slot] = np.arange(len(ref_row_slot))
-    assert np.array_equal(host["slot_row"].numpy(), slot_row)
-
-
-def check_stages_against_oracle(st, x_np, ids_np, tw_np, w_np, E, H, I):
-    """Each stage of a run_stages() result against the oracle fed the GPU's
-    own inputs for that stage."""
-    T, k = ids_np.shape
-    row_slot, offs, gexp = O.route_groups(ids_np, E)
-    check_groups(st["groups"], row_slot, offs, gexp, T * k)
-    R = len(row_slot)
-    xg = O.gather_rows(x_np, row_slot, k)
-    assert np.array_equal(bf16_to_np(st["xg"])[:R], xg)
-    xq, xsf = O.quantize_rows(xg, offs)
-    assert np.array_equal(st["xq"][:R].cpu().numpy(), xq)
-    want = chunk32_bytes(row_scales(xsf, offs, H), offs, H)
-    assert np.array_equal(st["xsf"][:want.size].cpu().numpy(), want)
-    d13 = O.grouped_gemm(xq, xsf, offs, gexp, w_np["w13_packed"], w_np["w13_sf_linear"])
-    assert rel_fro(st["d13"][:R].cpu().numpy(), d13) <= GEMM_TOL
-    h_ref = O.swiglu(st["d13"][:R].cpu().numpy().astype(np.float64), offs, gexp, w_np["g_gate_up"])
-    assert bf16_ulps(bf16_to_np(st["h"])[:R], h_ref).max() <= 1
-    h_gpu = bf16_to_np(st["h"])[:R]
-    hq, hsf = O.quantize_rows(h_gpu, offs)
-    assert np.array_equal(st["hq"][:R].cpu().numpy(), hq)
-    want = chunk32_bytes(row_scales(hsf, offs, I), offs, I)
-    assert np.array_equal(st["hsf"][:want.size].cpu().numpy(), want)
-    d2 = O.grouped_gemm(hq, hsf, offs, gexp, w_np["w2_packed"], w_np["w2_sf_linear"])
-    assert rel_fro(st["d2"][:R].cpu().numpy(), d2) <= GEMM_TOL
-    y_ref = O.scatter_add(st["d2"][:R].cpu().numpy().astype(np.float64), row_slot, ids_np, tw_np,
-                          w_np["g_down"], T, E)
-    assert bf16_ulps(bf16_to_np(st["y"]), y_ref).max() <= 1
 
 
 # ---------------------------------------------------------------------------
@@ -181,23 +132,6 @@ def _groups_for(mg, cuda):
     G = N.Groups(ids.shape[0], 1, len(mg), cuda)
     N.moe_route_groups(ids.to(cuda), len(mg), G)
     return ids, G
-
-
-def edge_rows(R, K, seed=0):
-    """bf16 rows mixing N(0,1), wide dynamic range, e2m1 ties, e4m3 subnormal
-    and saturating scales, all-zero and underflowing (signed) blocks."""
-    rng = np.random.default_rng(seed)
-    x = rng.standard_normal((R, K)).astype(np.float32)
-    x *= np.exp2(rng.integers(-14, 12, (R, K // 16))).repeat(16, axis=1).astype(np.float32)
-    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
-    for r in range(R):
-        c = 16 * int(rng.integers(0, K // 16))
-        x[r, c:c + 16] = np.tile(ties, 2) * rng.choice([-1, 1], 16)  # amax 6 -> scale 1, exact ties
-    x[0, :16] = 0.0
-    x[min(1, R - 1), :16] = -1e-7
-    x[min(2, R - 1), 16:32] = 5000.0                                    # scale saturates at 448
-    x[min(3, R - 1), 32:48] = 2.0 ** -9 * np.arange(16)                  # subnormal scale
-    return np.asarray(O.f64_to_bf16_bits(x.astype(np.float64)))
 
 
 @pytest.mark.parametrize("mg,K", [((1, 130), 64), ((3, 17, 1, 140), 256), ((1,), 4096), ((33, 64, 5), 1024)])
@@ -530,11 +464,28 @@ def _token_check(t, x_np, ids_np, tw_np, w_or, E, gpu_y, gpu_st=None):
     ref = O.moe_layer(x_np[t:t + 1], ids_np[t:t + 1], tw_np[t:t + 1], w_or, E)
     assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(gpu_y[t:t + 1])), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
     if gpu_st is not None:
+        # every stage of the token's rows at full size: K = 4096 for w13 and
+        # K = 2048 (eight stages, gated per stage on h in the layer) for w2
         k = ids_np.shape[1]
+        H2, I2 = gpu_st["xq"].shape[1], gpu_st["hq"].shape[1]
+        info = gpu_st["groups"]["chunk_info"].numpy()
         slot_row = gpu_st["groups"]["slot_row"].numpy()
-        rows = [slot_row[t * k + s] for s in ref["row_slot"]]
-        assert rel_fro(gpu_st["d13"][rows].cpu().numpy(), ref["d13"]) <= GEMM_TOL
+        rows = [int(slot_row[t * k + s]) for s in ref["row_slot"]]
+        offs1 = ref["group_offsets"]            # the token alone: one row per group
         assert np.array_equal(gpu_st["xq"][rows].cpu().numpy(), ref["xq"])
+        assert np.array_equal(chunk32_row_scales(gpu_st["xsf"].cpu().numpy(), info, rows, 2 * H2),
+                              row_scales(ref["xsf"], offs1, 2 * H2))
+        assert rel_fro(gpu_st["d13"][rows].cpu().numpy(), ref["d13"]) <= GEMM_TOL
+        # SwiGLU of the GPU's d13 within one bf16 ulp; requantization of the
+        # GPU's h bit-exact; w2 against the oracle fed those NVFP4 rows
+        h_gpu = bf16_to_np(gpu_st["h"])[rows]
+        assert_swiglu_close(h_gpu, gpu_st["d13"][rows].cpu().numpy(), offs1, ref["group_expert"], w_or["g_gate_up"])
+        hq, hsf = O.quantize_rows(h_gpu, offs1)
+        assert np.array_equal(gpu_st["hq"][rows].cpu().numpy(), hq)
+        assert np.array_equal(chunk32_row_scales(gpu_st["hsf"].cpu().numpy(), info, rows, 2 * I2),
+                              row_scales(hsf, offs1, 2 * I2))
+        d2 = O.grouped_gemm(hq, hsf, offs1, ref["group_expert"], w_or["w2_packed"], w_or["w2_sf_linear"])
+        assert rel_fro(gpu_st["d2"][rows].cpu().numpy(), d2) <= GEMM_TOL
 
 
 @pytest.mark.parametrize("name,tokens", [("decode_m1", (0,)), ("decode_m8", (0, 5)), ("decode_m32", (3, 31)),

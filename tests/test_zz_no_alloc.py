@@ -5,6 +5,8 @@ the same inputs, call after call, with the scratch array shared between calls.
 
 This file is collected last on purpose: a failure here leaves every other
 test already run."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -55,3 +57,28 @@ def test_static_layer_decode_sizes(cuda):
     assert N.load().moe_nvfp4_layer_workspace_size(32, 8, cfg.E, cfg.H, cfg.I) > N.STATIC_SCRATCH_BYTES
     with pytest.raises(RuntimeError, match="workspace too small"):
         N.moe_nvfp4_layer_static(x, ids.to(cuda), tw.to(cuda), W, torch.empty_like(x))
+
+
+def test_static_layer_at_its_size_limit(cuda):
+    """The largest decode batch whose workspace fits the scratch array runs and
+    equals the workspace entry point; one more token is rejected on the host
+    with MOE_ERR_WORKSPACE (status 5). The limit is derived from
+    moe_nvfp4_layer_workspace_size, the same function the entry point uses."""
+    cfg = CONFIGS["decode_m8"]
+    lib = N.load()
+    fits = [T for T in range(1, 64)
+            if lib.moe_nvfp4_layer_workspace_size(T, cfg.k, cfg.E, cfg.H, cfg.I) <= N.STATIC_SCRATCH_BYTES]
+    T_max = max(fits)
+    assert fits == list(range(1, T_max + 1))
+    assert lib.moe_nvfp4_layer_workspace_size(T_max + 1, cfg.k, cfg.E, cfg.H, cfg.I) > N.STATIC_SCRATCH_BYTES
+    w = make_weights(cfg.E, cfg.H, cfg.I, device=cuda)
+    W = weights_from(w)
+    del w
+    for T in (T_max, T_max + 1):
+        ids, tw = make_routing(dataclasses.replace(cfg, T=T))
+        x = make_activations(T, cfg.H, device=cuda)
+        if T == T_max:
+            _check_against_workspace_entry(x, ids.to(cuda), tw.to(cuda), W, cfg.k)
+        else:
+            with pytest.raises(RuntimeError, match="workspace too small"):
+                N.moe_nvfp4_layer_static(x, ids.to(cuda), tw.to(cuda), W, torch.empty_like(x))
