@@ -161,6 +161,7 @@ def gpu_bench(args, rank, world):
     from nvfp4_block_scaled_gather_gb300 import _native as N
     from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_activations, make_routing, make_weights
 
+    import dataclasses
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -174,7 +175,6 @@ def gpu_bench(args, rank, world):
 
     cfg = CONFIGS[args.config]
     if args.experts:
-        import dataclasses
         cfg = dataclasses.replace(cfg, E=args.experts)
     w = make_weights(cfg.E, cfg.H, cfg.I, device=dev)
     W = N.Weights(w["w13_packed"], w["w13_sf_linear"], w["g_gate_up"], w["w2_packed"], w["w2_sf_linear"],
@@ -201,11 +201,41 @@ def gpu_bench(args, rank, world):
         flush.zero_()
         flush_read.sum(dtype=torch.int32)
 
-    def time_layer(c, items, steps, warmup, sampler=None, graph=True):
+    warm_cache = {}
+
+    def code_warmer(c, T):
+        """A tiny layer step (8 experts, hidden 256, intermediate 128, weights
+        of its own) taking the same kernel paths as a step of T tokens of
+        config c: run after the L2 flush, untimed, it brings the kernels'
+        code back into L2 and leaves the timed step's weights, activations
+        and routing cold -- the state of a model whose every layer runs these
+        kernels with its own weights."""
+        S = T * c.k
+        lay = N.layer_sf_layout(T, c.k, c.E)
+        Tw = 1 if S <= 32 else (16 if lay == N.SF_ATOM128 else 8)
+        if Tw not in warm_cache:
+            tw_cfg = dataclasses.replace(CONFIGS["tiny"], E=8, k=8, T=Tw)
+            w8 = make_weights(8, 256, 128, seed=77, device=dev)
+            W8 = N.Weights(w8["w13_packed"], w8["w13_sf_linear"], w8["g_gate_up"], w8["w2_packed"],
+                           w8["w2_sf_linear"], w8["g_down"])
+            ids8, tw8 = make_routing(tw_cfg, seed=77)
+            x8 = make_activations(Tw, 256, seed=77, device=dev)
+            y8 = torch.empty_like(x8)
+            lay8 = N.MoeLayer(W8, Tw, 8)
+            assert N.layer_sf_layout(Tw, 8, 8) == lay
+            ids8, tw8 = ids8.to(dev), tw8.to(dev)
+            warm_cache[Tw] = (lay8.capture(x8, ids8, tw8, y8), W8, x8, ids8, tw8, y8, lay8)
+        return warm_cache[Tw][0]
+
+    def time_layer(c, items, steps, warmup, sampler=None, graph=True, code_warm=False):
         """Times `steps` layer steps (mean and per-step CUDA events), L2
         flushed before each. graph=True replays one CUDA graph per routing
-        (captured from the same C-ABI call); graph=False calls it directly."""
+        (captured from the same C-ABI call); graph=False calls it directly.
+        code_warm: after each flush, a tiny untimed step through the same
+        kernels (code_warmer) so their code is in L2 and only the data is
+        cold."""
         T_max = max(it["T"] for it in items)
+        warm = code_warmer(c, T_max) if code_warm else None
         layer = N.MoeLayer(W, T_max, c.k)
         ys = [torch.empty_like(it["x"]) for it in items]
         if graph:
@@ -233,6 +263,8 @@ def gpu_bench(args, rank, world):
         torch.cuda.synchronize()
         for i in range(steps):
             flush_l2()
+            if warm is not None:
+                warm.replay()
             ev[i][0].record(stream)
             run(i)
             ev[i][1].record(stream)
@@ -269,11 +301,12 @@ def gpu_bench(args, rank, world):
         events between them (per-kernel device time)."""
         T_max = max(it["T"] for it in items)
         S = T_max * c.k
+        lay = N.layer_sf_layout(T_max, c.k, c.E)  # the token blocks the layer itself takes
         G_ = N.Groups(T_max, c.k, c.E, dev)
         xq = torch.empty(S, c.H // 2, dtype=torch.uint8, device=dev)
-        xsf = torch.empty(N.sf_bytes(S, c.E, c.H, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
+        xsf = torch.empty(N.sf_bytes(S, c.E, c.H, lay), dtype=torch.uint8, device=dev)
         hq = torch.empty(S, c.I // 2, dtype=torch.uint8, device=dev)
-        hsf = torch.empty(N.sf_bytes(S, c.E, c.I, N.SF_CHUNK32), dtype=torch.uint8, device=dev)
+        hsf = torch.empty(N.sf_bytes(S, c.E, c.I, lay), dtype=torch.uint8, device=dev)
         d2 = torch.empty(S, c.H, dtype=torch.float32, device=dev)
         gate = torch.zeros(N.expert_gemms_gate_bytes(S, c.E, c.I), dtype=torch.uint8, device=dev)  # zeroed once
         names = ["route", "gather_quantize", "expert_gemms", "scatter"]
@@ -289,9 +322,9 @@ def gpu_bench(args, rank, world):
             evs[0].record(stream)
             N.moe_route_groups(it["ids"], c.E, G1)
             evs[1].record(stream)
-            N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf)
+            N.moe_gather_quantize_rows(it["x"], c.k, G1, xq, xsf, lay)
             evs[2].record(stream)
-            N.nvfp4_moe_expert_gemms(xq, xsf, G1, W, hq, hsf, d2, gate)
+            N.nvfp4_moe_expert_gemms(xq, xsf, G1, W, hq, hsf, d2, gate, layout=lay)
             evs[3].record(stream)
             N.moe_scatter_add(d2, it["ids"], it["tw"], c.E, G1, W.g_down, y)
             evs[4].record(stream)
@@ -372,6 +405,7 @@ def gpu_bench(args, rank, world):
     ms, byts = time_layer(cfg, items, args.steps, args.warmup, sampler, graph=not args.eager)
     clocks = sampler.stop()
     ms_eager, _ = time_layer(cfg, items, max(10, min(args.steps, 40)), 3, graph=False)
+    ms_warm, _ = time_layer(cfg, items, max(10, min(args.steps, 40)), 3, code_warm=True)
     total_ms = max_over_ranks(sum(ms), dist, dev)
     ms_step = total_ms / args.steps
     gbs = replica_throughput(world, sum(byts), total_ms)
@@ -416,6 +450,7 @@ def gpu_bench(args, rank, world):
         "ms_per_step_median": round(statistics.median(ms), 5),
         "step_launch": "eager C-ABI call" if args.eager else "CUDA graph of the C-ABI call (one per routing buffer set)",
         "ms_per_step_eager": round(statistics.mean(ms_eager), 5),
+        "ms_per_step_code_warm": round(statistics.mean(ms_warm), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -454,7 +489,7 @@ def gpu_bench(args, rank, world):
         "device": props.name,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(args.config)
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -465,15 +500,24 @@ def gpu_bench(args, rank, world):
 # CPU oracle (the reported baseline, and the reference arm)
 # ---------------------------------------------------------------------------
 
-ORACLE_SAMPLE_EXPERTS = 2
+def oracle_tasks(cfg_name, step_index):
+    """The oracle's work for one layer step of the config's first token: one
+    task per routed slot (the token's experts; for decode M=1 that is the
+    whole top-8 step). Returns (task list, algorithmic bytes of the step)."""
+    from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS, make_routing
+
+    cfg = CONFIGS[cfg_name]
+    ids, _ = make_routing(cfg, seed=2 + 1000 * step_index)
+    slots = [j for j in range(ids.shape[1]) if 0 <= int(ids[0, j]) < cfg.E]
+    return [(step_index, j) for j in slots], step_bytes(cfg, len(slots), 1)
 
 
-def oracle_sample_step(cfg_name, seed_index=0):
-    """One oracle layer step on a bounded sample of the workload: the first
-    token of a seeded routing with its first ORACLE_SAMPLE_EXPERTS routed
-    slots kept (about a second of single-core work), host weights generated
-    for just the experts it reaches (renumbered). Returns (algorithmic bytes
-    of the sample, seconds, description)."""
+def oracle_worker(cfg_name, worker, warm, timed, ready, go, done, out):
+    """One spawned process, one thread: prepares its tasks' inputs (one
+    synthetic expert's NVFP4 weights, seeded by the worker, reused by every
+    task, and each task's token row and router weight), then, between the
+    parent's barriers, runs the oracle's layer step of every task: that
+    token routed to that one expert."""
     import numpy as np
     import torch
 
@@ -481,68 +525,116 @@ def oracle_sample_step(cfg_name, seed_index=0):
     from oracle import nvfp4_moe as O
 
     cfg = CONFIGS[cfg_name]
-    ids, tw = make_routing(cfg, seed=2 + 1000 * seed_index)
-    ntok = 1
-    ids, tw = ids[:ntok].clone(), tw[:ntok]
-    kept = 0
-    for j in range(ids.shape[1]):
-        if 0 <= int(ids[0, j]) < cfg.E and kept < ORACLE_SAMPLE_EXPERTS:
-            kept += 1
-        else:
-            ids[0, j] = -1
-    used = sorted(set(int(e) for e in ids.flatten().tolist() if 0 <= e < cfg.E))
-    remap = {e: i for i, e in enumerate(used)}
-    ids_c = torch.tensor([[remap.get(int(e), -1) for e in row] for row in ids.tolist()], dtype=torch.int32)
-    w = make_weights(len(used), cfg.H, cfg.I, seed=3 + seed_index)
-    w_np = {k: v.numpy() for k, v in w.items()}
-    x = make_activations(ntok, cfg.H, seed=1 + 1000 * seed_index)
-    x_bits = x.view(torch.int16).numpy().view(np.uint16)
-    t0 = time.perf_counter()
-    O.moe_layer(x_bits, ids_c.numpy(), tw.numpy(), w_np, E=len(used))
-    sec = time.perf_counter() - t0
-    desc = (f"{ntok} token of {cfg_name} routed to {len(used)} experts (its first {len(used)} of top-{cfg.k}), "
-            f"hidden {cfg.H}, intermediate {cfg.I}: one oracle layer step per sample, 1 thread")
-    return step_bytes(cfg, len(used), ntok), sec, desc
+    w = {k: v.numpy() for k, v in make_weights(1, cfg.H, cfg.I, seed=3 + worker).items()}
+
+    def prepare(task):
+        step, j = task
+        ids, tw = make_routing(cfg, seed=2 + 1000 * step)
+        one = np.full((1, cfg.k), -1, np.int32)
+        one[0, j] = 0                                   # the slot's expert, renumbered 0
+        x = make_activations(1, cfg.H, seed=1 + 1000 * step).view(torch.int16).numpy().view(np.uint16)
+        return x, one, tw[:1].numpy()
+
+    warm_in = [prepare(t) for t in warm]
+    timed_in = [prepare(t) for t in timed]
+    for x, ids, tw in warm_in:
+        O.moe_layer(x, ids, tw, w, E=1)
+    ready.wait()
+    go.wait()                                           # the timed region starts for every worker at once
+    for x, ids, tw in timed_in:
+        O.moe_layer(x, ids, tw, w, E=1)
+    done.wait()
+    out.put(worker)
+
+
+def oracle_parallel(cfg_name, workers, steps, warmup):
+    """Times `steps` oracle layer steps (after `warmup`) of the config's first
+    token, every routed expert a task, tasks dealt round-robin over `workers`
+    spawned single-thread processes. Inputs are prepared before the timed
+    region; the wall clock runs from a barrier all workers wait at to the
+    last task done. Returns (bytes, seconds, description)."""
+    import multiprocessing as mp
+
+    warm_tasks, timed_tasks, total_bytes = [], [], 0
+    for i in range(warmup):
+        warm_tasks += oracle_tasks(cfg_name, i)[0]
+    for i in range(warmup, warmup + steps):
+        t, b = oracle_tasks(cfg_name, i)
+        timed_tasks += t
+        total_bytes += b
+    ctx = mp.get_context("spawn")
+    ready, go, done = ctx.Barrier(workers + 1), ctx.Barrier(workers + 1), ctx.Barrier(workers + 1)
+    out = ctx.Queue()
+    env_keep = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for v in env_keep:
+        os.environ[v] = "1"                             # one thread per worker (inherited at spawn)
+    procs = [ctx.Process(target=oracle_worker,
+                         args=(cfg_name, r, warm_tasks[r::workers], timed_tasks[r::workers], ready, go, done, out))
+             for r in range(workers)]
+    try:
+        for p in procs:
+            p.start()
+        ready.wait()
+        go.wait()
+        t0 = time.perf_counter()
+        done.wait()
+        sec = time.perf_counter() - t0
+        for p in procs:
+            p.join()
+    finally:
+        for v, val in env_keep.items():
+            if val is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = val
+    from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS
+    cfg = CONFIGS[cfg_name]
+    per = len(timed_tasks) // max(1, steps)
+    desc = (f"{steps} step(s) of {cfg_name}'s first token (top-{cfg.k}: {per} expert tasks per step, hidden "
+            f"{cfg.H}, intermediate {cfg.I}), each task the oracle's layer step for one routed expert, "
+            f"{workers} spawned single-thread process(es), tasks dealt round-robin")
+    return total_bytes, sec, desc
 
 
 def oracle_child(args):
-    """Runs in a child process with one BLAS/OpenMP thread."""
-    total_b, total_s, n, desc = 0, 0.0, 0, ""
-    t_start = time.time()
-    i = 0
-    while True:
-        b, s, desc = oracle_sample_step(args.config, i)
-        if i >= args.child_warmup:
-            total_b += b
-            total_s += s
-            n += 1
-        i += 1
-        if args.child_steps and n >= args.child_steps:
-            break
-        if not args.child_steps and time.time() - t_start > args.cpu_seconds and n >= 1:
-            break
-    print(json.dumps({"bytes": total_b, "seconds": total_s, "steps": n, "desc": desc}))
+    """Runs in a fresh process (no CUDA context): the parallel oracle timing."""
+    b, s, desc = oracle_parallel(args.config, args.child_workers, args.child_steps, args.child_warmup)
+    print(json.dumps({"bytes": b, "seconds": s, "steps": args.child_steps, "workers": args.child_workers,
+                      "desc": desc}))
 
 
-def run_oracle_child(config, seconds, steps=0, warmup=0):
+def run_oracle_child(config, workers, steps, warmup):
     env = dict(os.environ)
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[v] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--config", config,
-           "--cpu-seconds", str(seconds), "--child-steps", str(steps), "--child-warmup", str(warmup)]
+           "--child-workers", str(workers), "--child-steps", str(steps), "--child-warmup", str(warmup)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError(f"oracle timing failed:\n{r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline(config, seconds):
-    res = run_oracle_child(config, seconds)
-    gbs = res["bytes"] / res["seconds"] / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{res['steps']} step(s): {res['desc']}", "ms_per_step": round(1e3 * res["seconds"] / res["steps"], 1),
-            "cpu_model": cpu_model()}
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(config):
+    """The oracle on the host cores: all of them (one process per core, the
+    reported figure) and one (single_core), each over whole steps of the
+    config's first token (for decode M=1: the full top-8 step)."""
+    n = host_cores()
+    res = run_oracle_child(config, n, steps=max(2, (2 * n) // 8 * 2), warmup=1)
+    one = run_oracle_child(config, 1, steps=2, warmup=1)
+    entry = lambda r: {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": "GB/s",  # noqa: E731
+                       "cores": r["workers"], "kind": "oracle", "sample": r["desc"],
+                       "ms_per_step": round(1e3 * r["seconds"] / r["steps"], 1)}
+    out = entry(res)
+    out["cpu_model"] = cpu_model()
+    out["single_core"] = entry(one)
+    return out
 
 
 def cpu_model():
@@ -557,11 +649,15 @@ def cpu_model():
 
 
 def reference_arm(args, rank, world):
+    """The CPU oracle as the reference arm: the same metric on whole steps of
+    the config's first token (for decode M=1 the full top-8 step), on every
+    host core (one spawned process per core). Rank 0 only."""
     if rank != 0:
         return
     from nvfp4_block_scaled_gather_gb300.synthetic import CONFIGS
     cfg = CONFIGS[args.config]
-    res = run_oracle_child(args.config, args.cpu_seconds, steps=args.steps, warmup=args.warmup)
+    n = host_cores()
+    res = run_oracle_child(args.config, n, steps=args.steps, warmup=args.warmup)
     gbs = res["bytes"] / res["seconds"] / 1e9
     ms = 1e3 * res["seconds"] / res["steps"]
     sample = f"{res['steps']} timed step(s) after {args.warmup} warm-up: {res['desc']}"
@@ -581,7 +677,8 @@ def reference_arm(args, rank, world):
         "data": "synthetic",
         "config": {"workload": f"{cfg.name}: {cfg.E} experts, hidden {cfg.H}, intermediate {cfg.I}",
                    "sample": sample},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["workers"], "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -603,9 +700,9 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time direct calls instead of CUDA-graph replays")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--child-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--child-workers", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--child-steps", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--child-warmup", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup) if not args.oracle_child else args.warmup

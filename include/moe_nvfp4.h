@@ -46,6 +46,23 @@
  * (first page, "What changed": ordered map, batch-invariant group order).
  * Activation scale regions are laid out per group, each padded with zero bytes
  * to a multiple of 128 rows; packed rows are contiguous with no padding.
+ *
+ * Where these signatures depart from the plain per-step seams the first page
+ * names (packed weights plus a separate scale array per GEMM, group arrays as
+ * loose pointers):
+ *   - Weights reach the GEMMs pre-tiled (nvfp4_tile_weights, once at load
+ *     time: e2m1 bytes already in the MMA's shared-memory swizzle with each
+ *     256-value K stage's scales next to them, w13's gate and up rows
+ *     interleaved per 64), so one contiguous copy feeds one pipeline stage and
+ *     one accumulator holds both halves of a feature block for the fused
+ *     SwiGLU. It is the same idea as the pages' load-time scale swizzle, taken
+ *     one step further; the bytes are the same.
+ *   - The group metadata (offsets, expert ids, token-block tables, row/slot
+ *     maps) travels as one moe_groups_t filled on the device by the route
+ *     step, because every later step needs the same tables and the host never
+ *     sees them (no device-to-host sync in the step).
+ *   - The GEMM entry points take the token-scale layout, which fixes the token
+ *     block size a launch works in (32 or 128 rows).
  */
 #ifndef MOE_NVFP4_H
 #define MOE_NVFP4_H
@@ -67,17 +84,20 @@ enum {
   MOE_ERR_WORKSPACE = 5  /* workspace smaller than moe_nvfp4_layer_workspace_size() */
 };
 
-/* Token-scale layouts (the e4m3 scales of quantized activation rows).
- *   MOE_SF_ATOM128: per group, 128-row atoms as above, each group's region
- *     zero-padded to a multiple of 128 rows (the CUTLASS SFA layout the first
- *     page's kernels wrote; nvfp4_sf_bytes() bytes).
- *   MOE_SF_CHUNK32: what nvfp4_grouped_gemm reads. Rows of each group are cut
- *     into 32-row chunks (chunk c = counts-order index from group_chunk); for
- *     chunk c and K-atom a (64 values) a 512-byte block at (c*(K/64) + a)*512
- *     whose 16-byte row i holds, in its first 4 bytes, the scales of chunk row
- *     i for K-blocks 4a..4a+3; all other bytes are zero. Each block is what one
- *     tcgen05.cp.32x128b.warpx4 copies for a token operand of up to 32 rows.
- * Both regions are 128*(K/16) bytes per block (128-row atom or 32-row chunk). */
+/* Token-scale layouts (the e4m3 scales of quantized activation rows). Both
+ * cut each group's rows into blocks and give block b the region of 128*(K/16)
+ * bytes at b*128*(K/16), holding its rows in the atom layout above (row m of
+ * the block, scale column c at ((c/4)*512 + (m%32)*16 + ((m/32)%4)*4 + c%4);
+ * bytes no row fills are zero). They differ in the block size:
+ *   MOE_SF_ATOM128: 128-row blocks (block numbering group_sf_block /
+ *     block_info): the CUTLASS SFA layout, per group zero-padded to a multiple
+ *     of 128 rows, that the first page's kernels wrote.
+ *   MOE_SF_CHUNK32: 32-row blocks ("chunks", numbering group_chunk /
+ *     chunk_info): only rows 0..31 of each atom are used.
+ * The grouped GEMM takes the token operand in blocks of this size: one MMA of
+ * N = the block's rows (rounded up to 16) per 128-row weight tile, so every
+ * weight tile streams once per block. Its results are the same bits with
+ * either layout (a row's sums do not depend on the MMA width). */
 enum { MOE_SF_ATOM128 = 0, MOE_SF_CHUNK32 = 1 };
 
 /* Group metadata produced by moe_route_groups (device int32 arrays, caller
@@ -90,6 +110,9 @@ enum { MOE_SF_ATOM128 = 0, MOE_SF_CHUNK32 = 1 };
  *   group_chunk[E+1]     first 32-row GEMM chunk of group g; entry G = total
  *   chunk_info[4*C]      per 32-row chunk c: first grouped row, rows (1..32),
  *                        expert id, group; C = min(E, T*k) + ceil(T*k/32)
+ *   block_info[4*B]      per 128-row block b: first grouped row, rows
+ *                        (1..128), expert id, group; B = min(E, T*k) +
+ *                        ceil(T*k/128)
  *   row_slot[T*k]        slot t*k+j of grouped row r (r < R)
  *   slot_row[T*k]        grouped row of slot s, or -1 for an unused slot     */
 typedef struct {
@@ -99,6 +122,7 @@ typedef struct {
   int32_t* group_sf_block;
   int32_t* group_chunk;
   int32_t* chunk_info;
+  int32_t* block_info;
   int32_t* row_slot;
   int32_t* slot_row;
 } moe_groups_t;
@@ -182,43 +206,46 @@ int moe_route_gather_quantize(const int32_t* topk_ids, int T, int k, int E, cons
 /* a4 / a7 -- nvfp4_grouped_gemm: for every group g (expert e) and row r of
  * it, d[r, n] = sum_k A[r, k] * W[e, n, k] over dequantized values, no global
  * (alpha = 1), fp32 out, d [R_max, N] row-major (rows >= R untouched).
- * a_sf is in MOE_SF_CHUNK32. W [E, N, K] comes tiled by nvfp4_tile_weights;
- * w_interleaved says it was tiled with interleave_rows = N (columns of d are
- * in natural order either way). A group larger than 32 rows is processed as
- * ceil(Mg/32) chunks, each streaming the expert's weights (decode groups hold
- * at most a few dozen rows). One launch for all groups on
- * tcgen05 block-scaled MMA (kind::mxf4nvf4, scale vector 16), accumulators in
- * tensor memory. First page, "What changed": grouped GEMM w13 N=4096 K=4096
- * and w2 N=4096 K=2048, alpha = 1. N % 128 == 0, K % 64 == 0; every pointer
- * 16-byte aligned. */
-int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
+ * a_sf is in a_sf_layout; a group is processed in blocks of that layout's
+ * size (32 rows for MOE_SF_CHUNK32, 128 for MOE_SF_ATOM128), each block
+ * streaming the expert's weight tiles once: 128-row blocks for groups of
+ * many rows (prefill-sized batches), 32-row ones for decode batches, where
+ * more, smaller work units keep every SM busy. W [E, N, K] comes tiled by
+ * nvfp4_tile_weights; w_interleaved says it was tiled with interleave_rows =
+ * N (columns of d are in natural order either way). One launch for all
+ * groups on tcgen05 block-scaled MMA (kind::mxf4nvf4, scale vector 16),
+ * accumulators in tensor memory. First page, "What changed": grouped GEMM
+ * w13 N=4096 K=4096 and w2 N=4096 K=2048, alpha = 1. N % 128 == 0,
+ * K % 64 == 0; every pointer 16-byte aligned. */
+int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, int a_sf_layout, const moe_groups_t* groups,
                        int R_max, const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
                        cudaStream_t stream);
 
 /* a4 + a5 + a6 fused -- the w13 grouped GEMM with SwiGLU and requantization
- * in its epilogue: from the NVFP4 rows (a_sf in MOE_SF_CHUNK32) and w13 tiled
+ * in its epilogue: from the NVFP4 rows (a_sf in a_sf_layout) and w13 tiled
  * with interleave_rows = 2I, writes NVFP4 h: packed [R_max, I/2] and token
- * scales h_sf (MOE_SF_CHUNK32, nvfp4_sf_bytes(R_max, E, I, 1) bytes). The
- * fp32 gate|up product never leaves the chip. Bit-identical to
+ * scales h_sf (the same layout, nvfp4_sf_bytes(R_max, E, I, a_sf_layout)
+ * bytes). The fp32 gate|up product never leaves the chip. Bit-identical to
  * nvfp4_grouped_gemm + swiglu_grouped + nvfp4_quantize_rows. The second
  * page's "SwiGLU as an epilogue" found this inexpressible in CUTLASS grouped
  * GEMM; per-half globals are still applied in registers (option (a)).
  * I % 128 == 0, K % 64 == 0. */
-int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups,
-                              int R_max, const uint8_t* w13_tiled, int E, int I, int K, const float* g_gate_up,
-                              uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream);
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, int a_sf_layout,
+                              const moe_groups_t* groups, int R_max, const uint8_t* w13_tiled, int E, int I, int K,
+                              const float* g_gate_up, uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream);
 
 /* a4 .. a7 in one persistent launch -- both grouped GEMMs of the layer: the
  * w13 GEMM with SwiGLU and requantization in its epilogue (as
  * nvfp4_grouped_gemm_swiglu, writing h_packed/h_sf) and the w2 GEMM reading
  * that h (as nvfp4_grouped_gemm into d2 [R_max, H] fp32). Each 256-wide K
- * stage of a 32-row chunk's w2 work starts once the four w13 tiles writing
+ * stage of a token block's w2 work starts once the four w13 tiles writing
  * those h features are done, so w2's weights stream, and its first stages
  * run, while w13 finishes. This is the launch
  * moe_nvfp4_layer makes between quantization and the scatter-add; the pages
  * ran the two GEMMs as separate launches (second page, "Fusing the MoE
  * layer's two grouped GEMMs is worth 4%").
- * x_packed/x_sf: NVFP4 token rows [R_max, H/2] and MOE_SF_CHUNK32 scales.
+ * x_packed/x_sf: NVFP4 token rows [R_max, H/2] and their scales in
+ * sf_layout; h_sf is written in the same layout.
  * gate: moe_expert_gemms_gate_bytes(R_max, E, I) bytes of device scratch for
  * the launch's work counters. Zero it once before the first call; a call
  * that completes leaves it zero. After an error (e.g. MOE_ERR_TIMEOUT from
@@ -226,9 +253,9 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
  * concurrently.
  * H % 128 == 0, I % 128 == 0. */
 size_t moe_expert_gemms_gate_bytes(int R_max, int E, int I);
-int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const moe_groups_t* groups, int R_max,
-                           const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed, uint8_t* h_sf,
-                           float* d2, void* gate, cudaStream_t stream);
+int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, int sf_layout, const moe_groups_t* groups,
+                           int R_max, const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed,
+                           uint8_t* h_sf, float* d2, void* gate, cudaStream_t stream);
 
 /* a5 -- swiglu_grouped: h[r, n] = silu(d13[r, n]*g_gate[e]) * (d13[r, I+n]*g_up[e]),
  * computed in fp32 (CUDA expf) and rounded once to bf16. d13 [R_max, 2I]
@@ -259,12 +286,22 @@ int moe_scatter_add(const float* d2, int H, const int32_t* topk_ids, const float
  * outputs). */
 size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I);
 
+/* The token-scale layout (token block size) moe_nvfp4_layer uses for T
+ * tokens, top-k, E experts: MOE_SF_ATOM128 (128-row blocks) when the batch
+ * routes at least 16 rows per expert on average (T*k >= 16*E, prefill-sized:
+ * weight tiles then stream once per 128 rows instead of once per 32), else
+ * MOE_SF_CHUNK32. A shape rule, not a fallback: the output bits are the same
+ * either way. A caller composing the step from the separate entry points can
+ * use it to match the layer's choice. */
+int moe_nvfp4_layer_sf_layout(int T, int k, int E);
+
 /* The whole step a1..a8 on `stream`: route-group, gather+quantize, grouped
  * GEMM w13 with SwiGLU+requantize in its epilogue, grouped GEMM w2,
  * scatter-add. Four launches for T*k > 32 (route, gather+quantize, both
  * GEMMs in one persistent launch, scatter), three for decode-sized batches
  * (T*k <= 32: route + gather + quantize in one). Each launch may start while
- * the previous one finishes (programmatic dependent launch).
+ * the previous one finishes (programmatic dependent launch). Token rows go
+ * through the GEMMs in blocks of moe_nvfp4_layer_sf_layout(T, k, E).
  * x [T, H] bf16, y [T, H] bf16 (overwritten). `workspace` is caller device
  * memory of ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I),
  * 256-byte aligned (any contents). Calls sharing a workspace run in stream

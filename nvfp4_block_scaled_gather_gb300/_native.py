@@ -24,7 +24,7 @@ SF_CHUNK32 = 1   # per 32-row chunk, the layout nvfp4_grouped_gemm reads
 
 class MoeGroups(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("counts", "group_offsets", "group_expert", "group_sf_block",
-                                       "group_chunk", "chunk_info", "row_slot", "slot_row")]
+                                       "group_chunk", "chunk_info", "block_info", "row_slot", "slot_row")]
 
 
 class MoeWeights(ctypes.Structure):
@@ -45,15 +45,16 @@ _SIGS = {
                                     c_void_p, c_void_p]),
     "moe_gather_quantize_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
                                          c_void_p, c_void_p, c_void_p]),
-    "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int, c_int,
-                                   c_int, c_int, c_void_p, c_void_p]),
-    "nvfp4_grouped_gemm_swiglu": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int,
-                                          c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nvfp4_grouped_gemm": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeGroups), c_int, c_void_p, c_int,
+                                   c_int, c_int, c_int, c_void_p, c_void_p]),
+    "nvfp4_grouped_gemm_swiglu": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeGroups), c_int, c_void_p,
+                                          c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_route_gather_quantize": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_int, ctypes.POINTER(MoeGroups),
                                           c_void_p, c_void_p, c_void_p]),
     "moe_expert_gemms_gate_bytes": (ctypes.c_size_t, [c_int, c_int, c_int]),
-    "nvfp4_moe_expert_gemms": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MoeGroups), c_int, ctypes.POINTER(MoeWeights),
-                                       c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "nvfp4_moe_expert_gemms": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MoeGroups), c_int,
+                                       ctypes.POINTER(MoeWeights), c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_void_p]),
     "swiglu_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_void_p, c_void_p,
                                c_void_p]),
     "swiglu_quantize_grouped": (c_int, [c_void_p, c_int, c_int, c_int, ctypes.POINTER(MoeGroups), c_int,
@@ -61,6 +62,7 @@ _SIGS = {
     "moe_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                 ctypes.POINTER(MoeGroups), c_void_p, c_void_p, c_void_p]),
     "moe_nvfp4_layer_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "moe_nvfp4_layer_sf_layout": (c_int, [c_int, c_int, c_int]),
     "moe_nvfp4_layer": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                 ctypes.POINTER(MoeWeights), c_void_p, c_size_t, c_void_p, c_void_p]),
     "nvfp4_swizzle_block_scales": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
@@ -146,6 +148,7 @@ class Groups:
                     group_sf_block=self.view("group_sf_block", G + 1).cpu(),
                     group_chunk=self.view("group_chunk", G + 1).cpu(),
                     chunk_info=self.view("chunk_info", 4 * nchunk).cpu().reshape(-1, 4),
+                    block_info=self.view("block_info", 4 * nblk).cpu().reshape(-1, 4),
                     row_slot=self.view("row_slot", R).cpu(),
                     slot_row=self.view("slot_row", S).cpu())
 
@@ -202,22 +205,23 @@ class TiledWeight:
                                          self.N if interleave else 0, _ptr(self.data), _stream(stream)))
 
 
-def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w: TiledWeight, d, stream=None):
+def nvfp4_grouped_gemm(a_packed, a_sf, groups: Groups, w: TiledWeight, d, layout: int = SF_CHUNK32, stream=None):
+    """a_sf in `layout`: the token block size the GEMM works in (32 or 128 rows)."""
     R_max = a_packed.shape[0]
     K = a_packed.shape[1] * 2
     assert K == w.K
     _check("nvfp4_grouped_gemm",
-           load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max, _ptr(w.data),
-                                     int(w.interleaved), w.E, w.N, K, _ptr(d), _stream(stream)))
+           load().nvfp4_grouped_gemm(_ptr(a_packed), _ptr(a_sf), layout, ctypes.byref(groups.struct), R_max,
+                                     _ptr(w.data), int(w.interleaved), w.E, w.N, K, _ptr(d), _stream(stream)))
 
 
 def nvfp4_grouped_gemm_swiglu(a_packed, a_sf, groups: Groups, w13: TiledWeight, g_gate_up, h_packed, h_sf,
-                              stream=None):
+                              layout: int = SF_CHUNK32, stream=None):
     R_max = a_packed.shape[0]
     K = a_packed.shape[1] * 2
     assert K == w13.K and w13.interleaved
     _check("nvfp4_grouped_gemm_swiglu",
-           load().nvfp4_grouped_gemm_swiglu(_ptr(a_packed), _ptr(a_sf), ctypes.byref(groups.struct), R_max,
+           load().nvfp4_grouped_gemm_swiglu(_ptr(a_packed), _ptr(a_sf), layout, ctypes.byref(groups.struct), R_max,
                                             _ptr(w13.data), w13.E, w13.N // 2, K, _ptr(g_gate_up), _ptr(h_packed),
                                             _ptr(h_sf), _stream(stream)))
 
@@ -230,11 +234,13 @@ def moe_route_gather_quantize(topk_ids, x, E: int, groups: Groups, packed, sf, s
                                             ctypes.byref(groups.struct), _ptr(packed), _ptr(sf), _stream(stream)))
 
 
-def nvfp4_moe_expert_gemms(x_packed, x_sf, groups: Groups, W: "Weights", h_packed, h_sf, d2, gate, stream=None):
-    """Both grouped GEMMs in one launch (w13 + SwiGLU + requantize, then w2)."""
+def nvfp4_moe_expert_gemms(x_packed, x_sf, groups: Groups, W: "Weights", h_packed, h_sf, d2, gate,
+                           layout: int = SF_CHUNK32, stream=None):
+    """Both grouped GEMMs in one launch (w13 + SwiGLU + requantize, then w2);
+    x_sf and h_sf in `layout`."""
     R_max = x_packed.shape[0]
     _check("nvfp4_moe_expert_gemms",
-           load().nvfp4_moe_expert_gemms(_ptr(x_packed), _ptr(x_sf), ctypes.byref(groups.struct), R_max,
+           load().nvfp4_moe_expert_gemms(_ptr(x_packed), _ptr(x_sf), layout, ctypes.byref(groups.struct), R_max,
                                          ctypes.byref(W.struct), W.H, W.I, _ptr(h_packed), _ptr(h_sf), _ptr(d2),
                                          _ptr(gate), _stream(stream)))
 
@@ -273,6 +279,11 @@ def nvfp4_swizzle_block_scales(linear, swizzled, stream=None):
 
 def moe_nvfp4_layer_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int:
     return load().moe_nvfp4_layer_workspace_size(T, k, E, H, I)
+
+
+def layer_sf_layout(T: int, k: int, E: int) -> int:
+    """The token-scale layout (token block size) moe_nvfp4_layer uses."""
+    return load().moe_nvfp4_layer_sf_layout(T, k, E)
 
 
 class Weights:

@@ -75,7 +75,8 @@ cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzle
 
 // tcgen05 grouped GEMM (nvfp4_gemm.cu), one persistent launch over one or
 // two jobs. A job: token rows a_packed [R_max, K/2] with token scales a_sf
-// (MOE_SF_CHUNK32), tiled weights [E, N, K], fp32 output d [R_max, N].
+// (in `layout`: MOE_SF_CHUNK32 = 32-row token blocks, MOE_SF_ATOM128 =
+// 128-row token blocks), tiled weights [E, N, K], fp32 output d [R_max, N].
 // w_interleaved: each 128-row weight tile holds 64 rows of the first half of
 // N and the matching 64 rows of the second half (nvfp4_tile_weights with
 // interleave); d still gets natural column order.
@@ -84,11 +85,11 @@ cudaError_t launch_swizzle(const uint8_t* linear, int N, int K, uint8_t* swizzle
 // (packed [R_max, I/2], token scales MOE_SF_CHUNK32), bit-identical to
 // swiglu_grouped followed by nvfp4_quantize_rows; job 0's d is not written.
 // j1 != nullptr: job 1 runs in the same launch and may read what job 0
-// wrote: a job-1 unit of a 32-row chunk starts its token loads once all of
+// wrote: a job-1 unit of a token block starts its token loads once all of
 // job 0's tiles writing that stage's features are done. gate holds
 // gate_ints(R_max, E, K1) ints, zero at launch: the unit claim counter, the
-// count of finished CTAs, then per (chunk, job-1 K stage of 256) the count of
-// finished job-0 tiles. The last CTA to finish zeroes them again, so a launch
+// count of finished CTAs, then per (token block, job-1 K stage of 256) the
+// count of finished job-0 tiles. The last CTA to finish zeroes them again, so a launch
 // that completes leaves gate ready for the next.
 // early: the group metadata, gate and the weights were written two or more
 // launches back (true inside moe_nvfp4_layer), so the GEMM may read them and
@@ -119,9 +120,17 @@ struct SmallFront {
   const int32_t* topk_ids;
   int S;
 };
-cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
-                                const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
-                                cudaStream_t s);
+// front requires layout == MOE_SF_CHUNK32.
+cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, int layout, const GemmJob& j0,
+                                const SwigluOut* swiglu, const GemmJob* j1, int* gate, const SmallFront* front,
+                                bool early, int* status, cudaStream_t s);
+
+// The layer's token block size for S = T*k slots over E experts: 128-row
+// blocks (MOE_SF_ATOM128) when S >= 16*E (and the batch is not decode-sized),
+// else 32-row chunks.
+inline int layer_sf_layout(long long S, long long E) {
+  return (S > kSmallRouteSlots && S >= 16 * E) ? MOE_SF_ATOM128 : MOE_SF_CHUNK32;
+}
 
 // W4A16 grouped GEMV (nvfp4_gemv.cu): d [R_max, N] fp32 = bf16 rows times the
 // group's expert's tiled NVFP4 weight [E, N, K] (no global); rows are

@@ -48,7 +48,7 @@ bool misaligned(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 != 0
 
 bool groups_ok(const moe_groups_t* g) {
   return g && g->counts && g->group_offsets && g->group_expert && g->group_sf_block && g->group_chunk &&
-         g->chunk_info && g->row_slot && g->slot_row;
+         g->chunk_info && g->block_info && g->row_slot && g->slot_row;
 }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -59,7 +59,7 @@ struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
   float* d2;
-  int* gate;  // the GEMM's unit claim counter, then w13 tiles finished per 32-row chunk
+  int* gate;  // the GEMM's unit claim counter, finished CTAs, then w13 tiles finished per token block
   int ngate;
   size_t bytes;
 };
@@ -79,9 +79,10 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   uint8_t* gmem = take(moe_groups_bytes(T, k, E));
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
-  w.xsf = take(token_sf_bytes((long long)S, E, H, MOE_SF_CHUNK32));
+  const int layout = layer_sf_layout((long long)S, E);
+  w.xsf = take(token_sf_bytes((long long)S, E, H, layout));
   w.hq = take(S * I / 2);
-  w.hsf = take(token_sf_bytes((long long)S, E, I, MOE_SF_CHUNK32));
+  w.hsf = take(token_sf_bytes((long long)S, E, I, layout));
   w.d2 = reinterpret_cast<float*>(take(S * H * sizeof(float)));
   w.bytes = off;
   return w;
@@ -177,7 +178,7 @@ size_t moe_groups_bytes(int T, int k, int E) {
   const size_t S = (size_t)T * k;
   return align256(16 * 4) + align256(4 * (size_t)(E + 1)) + align256(4 * (size_t)E) +
          2 * align256(4 * (size_t)(E + 1)) + align256(16 * (size_t)chunks_bound((long long)S, E)) +
-         2 * align256(4 * S);
+         align256(16 * (size_t)sf_blocks_bound((long long)S, E)) + 2 * align256(4 * S);
 }
 
 int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
@@ -191,6 +192,7 @@ int moe_groups_carve(void* mem, int T, int k, int E, moe_groups_t* g) {
   g->group_sf_block = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
   g->group_chunk = reinterpret_cast<int32_t*>(p); p += align256(4 * (size_t)(E + 1));
   g->chunk_info = reinterpret_cast<int32_t*>(p); p += align256(16 * (size_t)chunks_bound((long long)S, E));
+  g->block_info = reinterpret_cast<int32_t*>(p); p += align256(16 * (size_t)sf_blocks_bound((long long)S, E));
   g->row_slot = reinterpret_cast<int32_t*>(p); p += align256(4 * S);
   g->slot_row = reinterpret_cast<int32_t*>(p);
   return MOE_OK;
@@ -258,10 +260,11 @@ int moe_route_gather_quantize(const int32_t* topk_ids, int T, int k, int E, cons
   return status_of(err);
 }
 
-int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
-                       const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
+int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, int a_sf_layout, const moe_groups_t* groups,
+                       int R_max, const uint8_t* w_tiled, int w_interleaved, int E, int N, int K, float* d,
                        cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID;
+  if (!groups_ok(groups) || R_max < 0 || E <= 0 || N <= 0 || K <= 0 || !layout_ok(a_sf_layout))
+    return MOE_ERR_INVALID;
   if (N % 128 || K % 64 || (w_interleaved && N % 256)) return MOE_ERR_SHAPE;
   if ((long long)E * N > (1LL << 31)) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
@@ -272,13 +275,15 @@ int nvfp4_grouped_gemm(const uint8_t* a_packed, const uint8_t* a_sf, const moe_g
   int* st = status_ptr();
   if (!st) return MOE_ERR_CUDA;
   const GemmJob job{a_packed, a_sf, w_tiled, w_interleaved != 0, N, K, d};
-  return status_of(launch_grouped_gemm(*groups, R_max, E, job, nullptr, nullptr, nullptr, nullptr, false, st, stream));
+  return status_of(
+      launch_grouped_gemm(*groups, R_max, E, a_sf_layout, job, nullptr, nullptr, nullptr, nullptr, false, st, stream));
 }
 
-int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, const moe_groups_t* groups, int R_max,
-                              const uint8_t* w13_tiled, int E, int I, int K, const float* g_gate_up,
-                              uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream) {
-  if (!groups_ok(groups) || R_max < 0 || E <= 0 || I <= 0 || K <= 0) return MOE_ERR_INVALID;
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, int a_sf_layout,
+                              const moe_groups_t* groups, int R_max, const uint8_t* w13_tiled, int E, int I, int K,
+                              const float* g_gate_up, uint8_t* h_packed, uint8_t* h_sf, cudaStream_t stream) {
+  if (!groups_ok(groups) || R_max < 0 || E <= 0 || I <= 0 || K <= 0 || !layout_ok(a_sf_layout))
+    return MOE_ERR_INVALID;
   if (I % 128 || K % 64) return MOE_ERR_SHAPE;
   if ((long long)E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
   if (R_max == 0) return MOE_OK;
@@ -291,7 +296,8 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a_packed, const uint8_t* a_sf, cons
   if (!st) return MOE_ERR_CUDA;
   const SwigluOut out{h_packed, h_sf, g_gate_up};
   const GemmJob job{a_packed, a_sf, w13_tiled, true, 2 * I, K, nullptr};
-  return status_of(launch_grouped_gemm(*groups, R_max, E, job, &out, nullptr, nullptr, nullptr, false, st, stream));
+  return status_of(
+      launch_grouped_gemm(*groups, R_max, E, a_sf_layout, job, &out, nullptr, nullptr, nullptr, false, st, stream));
 }
 
 size_t moe_expert_gemms_gate_bytes(int R_max, int E, int I) {
@@ -299,10 +305,11 @@ size_t moe_expert_gemms_gate_bytes(int R_max, int E, int I) {
   return (size_t)gate_ints(R_max, E, I) * sizeof(int);
 }
 
-int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const moe_groups_t* groups, int R_max,
-                           const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed, uint8_t* h_sf, float* d2,
-                           void* gate, cudaStream_t stream) {
-  if (!w || !groups_ok(groups) || R_max < 0 || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts)
+int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, int sf_layout, const moe_groups_t* groups,
+                           int R_max, const moe_nvfp4_weights_t* w, int H, int I, uint8_t* h_packed, uint8_t* h_sf,
+                           float* d2, void* gate, cudaStream_t stream) {
+  if (!w || !groups_ok(groups) || R_max < 0 || H <= 0 || I <= 0 || w->E <= 0 || w->E > kMaxExperts ||
+      !layout_ok(sf_layout))
     return MOE_ERR_INVALID;
   if (H % 128 || I % 128) return MOE_ERR_SHAPE;
   if ((long long)w->E * 2 * I > (1LL << 31)) return MOE_ERR_SHAPE;
@@ -319,8 +326,8 @@ int nvfp4_moe_expert_gemms(const uint8_t* x_packed, const uint8_t* x_sf, const m
   const GemmJob w13{x_packed, x_sf, w->w13_tiled, true, 2 * I, H, nullptr};
   const GemmJob w2{h_packed, h_sf, w->w2_tiled, false, H, I, d2};
   return status_of(
-      launch_grouped_gemm(*groups, R_max, E, w13, &swiglu, &w2, static_cast<int*>(gate), nullptr, false, st,
-                          stream));
+      launch_grouped_gemm(*groups, R_max, E, sf_layout, w13, &swiglu, &w2, static_cast<int*>(gate), nullptr, false,
+                          st, stream));
 }
 
 int swiglu_grouped(const float* d13, int R_max, int I, int E, const moe_groups_t* groups, const float* g_gate_up,
@@ -360,6 +367,11 @@ size_t moe_nvfp4_layer_workspace_size(int T, int k, int E, int H, int I) {
   return carve_layer(nullptr, T, k, E, H, I).bytes;
 }
 
+int moe_nvfp4_layer_sf_layout(int T, int k, int E) {
+  if (T < 0 || k < 0 || E <= 0) return MOE_SF_CHUNK32;
+  return layer_sf_layout((long long)T * k, E);
+}
+
 int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids, const float* topk_w, int k,
                     const moe_nvfp4_weights_t* w, void* workspace, size_t ws_bytes, uint16_t* y,
                     cudaStream_t stream) {
@@ -379,13 +391,15 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   // launch starts on weights before the previous kernel ends: with a group table two launches
   // old it claims units and streams them (early); for decode-sized batches it routes the
   // slots itself from topk_ids and warms L2 with its first weight stages while it waits.
+  // Token blocks (and scale layout): 128 rows for prefill-sized batches, else 32.
   const bool small = S <= kSmallRouteSlots;
+  const int layout = layer_sf_layout(S, E);
   cudaError_t err;
   if (small) {
     err = launch_route_quantize_small(topk_ids, S, E, ws.groups, ws.gate, ws.ngate, x, k, H, ws.xq, ws.xsf, stream);
   } else {
     err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate);
-    if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, MOE_SF_CHUNK32, ws.xq, ws.xsf, stream);
+    if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, layout, ws.xq, ws.xsf, stream);
   }
   const SmallFront front{topk_ids, S};
   // a4 + a5 + a6 (w13 with SwiGLU and requantization in its epilogue) and a7
@@ -394,8 +408,8 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   const GemmJob w13{ws.xq, ws.xsf, w->w13_tiled, true, 2 * I, H, nullptr};
   const GemmJob w2{ws.hq, ws.hsf, w->w2_tiled, false, H, I, ws.d2};
   if (err == cudaSuccess)
-    err = launch_grouped_gemm(ws.groups, S, E, w13, &swiglu, &w2, ws.gate, small ? &front : nullptr, !small, st,
-                              stream);
+    err = launch_grouped_gemm(ws.groups, S, E, layout, w13, &swiglu, &w2, ws.gate, small ? &front : nullptr, !small,
+                              st, stream);
   if (err == cudaSuccess)  // its routing tables are two or more launches old
     err = launch_scatter(ws.d2, H, topk_ids, topk_w, T, k, E, ws.groups, w->g_down, y, stream, true);
   return status_of(err);

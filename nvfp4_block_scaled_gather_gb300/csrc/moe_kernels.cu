@@ -24,16 +24,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ int find_group(const int32_t* __restrict__ starts, int G, int key) {
-  // largest g in [0, G) with starts[g] <= key; starts strictly ascending from 0
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ld_cg(starts + mid) <= key) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // ---------------------------------------------------------------------------
 // a1 route-group: one CTA of 1024 threads. Warp w owns the contiguous slot
 // range [s0, s1); per-(warp, expert) counts give every slot its row without
@@ -114,6 +104,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
       g.group_chunk[gi] = chk0;
       for (int q = 0; q < own3; ++q)  // the group's 32-row chunks
         reinterpret_cast<int4*>(g.chunk_info)[chk0 + q] = make_int4(row0 + 32 * q, min(32, cnt - 32 * q), tid, gi);
+      for (int q = 0; q < own2; ++q)  // and its 128-row blocks
+        reinterpret_cast<int4*>(g.block_info)[blk0 + q] = make_int4(row0 + 128 * q, min(128, cnt - 128 * q), tid, gi);
     }
   }
   if (tid == 0) {
@@ -195,6 +187,42 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
   if ((lane & 15) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
+// e2m1 codes of two fp32 values, round to nearest even, saturating at 6: the
+// hardware conversion (the same rounding as e2m1_encode, sign of zero kept);
+// `lo` goes to the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t b;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(b)
+      : "f"(hi), "f"(lo));
+  return b;
+}
+
+// Lane pairs (2j, 2j+1) of a warp hold one 16-value block, eight values each;
+// eight lanes hold the four blocks of one 4-byte scale word. Each lane writes
+// its four packed bytes; the first lane of each eight writes the word. Lanes
+// that are not `active` compute along (shuffles need the full warp) but write
+// nothing; an 8-lane group is either wholly active or wholly not.
+__device__ __forceinline__ void quantize_oct_store(const float (&v)[8], bool active, int lane,
+                                                   uint8_t* __restrict__ packed_dst, uint32_t* __restrict__ word) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+  const uint32_t s = e4m3_encode(__fdiv_rn(amax, 6.0f));
+  const float d = e4m3_decode(s);
+  uint32_t codes = 0u;
+  if (d != 0.0f) {  // an underflowed block keeps all-zero codes
+#pragma unroll
+    for (int i = 0; i < 4; ++i) codes |= e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d)) << (8 * i);
+  }
+  const uint32_t s1 = __shfl_down_sync(~0u, s, 2), s2 = __shfl_down_sync(~0u, s, 4),
+                 s3 = __shfl_down_sync(~0u, s, 6);
+  if (!active) return;
+  *reinterpret_cast<uint32_t*>(packed_dst) = codes;
+  if ((lane & 7) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
 // Token-scale layouts (include/moe_nvfp4.h): per group 128-row atoms, or per
 // 32-row GEMM chunk one 512-byte atom per 64 K values whose 16-byte row i
 // holds chunk row i's four scales in its first word (other words zero).
@@ -226,36 +254,28 @@ struct RowBlock {
   int row0, nvalid, expert;
 };
 
+__device__ __forceinline__ const int4* block_table(const moe_groups_t& g, int layout) {
+  return reinterpret_cast<const int4*>(layout == MOE_SF_CHUNK32 ? g.chunk_info : g.block_info);
+}
+
+// One table read, the same value in every thread.
 __device__ __forceinline__ RowBlock resolve_block(const moe_groups_t& g, int layout, int blk) {
-  if (layout == MOE_SF_CHUNK32) {  // one table read, same value in every thread
-    const int4 c = ld_cg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
-    return RowBlock{c.x, c.y, c.z};
-  }
-  __shared__ int s_info[3];
-  if (threadIdx.x == 0) {
-    const int G = ld_cg(g.counts + 0);
-    const int gi = find_group(g.group_sf_block, G, blk);
-    const int m0 = (blk - ld_cg(g.group_sf_block + gi)) * kRowsAtom;
-    const int r0 = ld_cg(g.group_offsets + gi);
-    const int mg = ld_cg(g.group_offsets + gi + 1) - r0;
-    s_info[0] = r0 + m0;
-    s_info[1] = min(kRowsAtom, mg - m0);
-    s_info[2] = ld_cg(g.group_expert + gi);
-  }
-  __syncthreads();
-  return RowBlock{s_info[0], s_info[1], s_info[2]};
+  const int4 c = ld_cg(block_table(g, layout) + blk);
+  return RowBlock{c.x, c.y, c.z};
 }
 
 __device__ __forceinline__ int routed_blocks(const moe_groups_t& g, int layout) {
   return ld_cg(g.counts + (layout == MOE_SF_ATOM128 ? 3 : 4));
 }
 
-constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K)
+constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K) for the SwiGLU and small-batch kernels
+constexpr int kQuantCols = 256;    // K values per CTA of the quantizer
 
 // ---------------------------------------------------------------------------
-// a3 / a6 quantize (with optional a2 gather). Grid: (row block, 1024-value
-// column chunk); CTAs past the routed block count exit. Each lane quantizes 4
-// values; scale words no real row fills are zeroed.
+// a3 / a6 quantize (with optional a2 gather). Grid: (row block, 256-value
+// column chunk); CTAs past the routed block count exit. Each lane quantizes 8
+// values from one 16-byte load, a lane pair one 16-value block; scale words no
+// real row fills are zeroed.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k, int K,
                                                             moe_groups_t g, int layout, uint8_t* __restrict__ packed,
@@ -263,22 +283,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
   const int blk = blockIdx.x;
-  RowBlock rb;
-  if (layout == MOE_SF_CHUNK32) {
-    // the block count and this block's table entry in flight together (the
-    // entry is in bounds whether or not the block is routed)
-    const int4 c = ld_cg(reinterpret_cast<const int4*>(g.chunk_info) + blk);
-    if (blk >= routed_blocks(g, layout)) return;
-    rb = RowBlock{c.x, c.y, c.z};
-  } else {
-    if (blk >= routed_blocks(g, layout)) return;
-    rb = resolve_block(g, layout, blk);
-  }
+  // the block count and this block's table entry in flight together (the
+  // entry is in bounds whether or not the block is routed)
+  const int4 c = ld_cg(block_table(g, layout) + blk);
+  if (blk >= routed_blocks(g, layout)) return;
+  const RowBlock rb{c.x, c.y, c.z};
   const int Kc = K / 16;
-  const int kc0 = blockIdx.y * kColsPerCta;
-  const int kcount = min(kColsPerCta, K - kc0);
-  const int quads = kcount / 4;
-  const int total = rb.nvalid * quads;
+  const int kc0 = blockIdx.y * kQuantCols;
+  const int kcount = min(kQuantCols, K - kc0);
+  const int octs = kcount / 8;
+  const int total = rb.nvalid * octs;
   const int lane = threadIdx.x & 31;
   const ScaleTarget st{sf + (size_t)blk * 128 * Kc, layout, Kc};  // either layout: 128*Kc bytes per block
   // source row of each of the block's rows, read once
@@ -290,16 +304,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   __syncthreads();
   // Up to kBatch of this warp's items loaded before any is quantized, so that
   // a block of many rows costs one memory round trip per kBatch, not per row.
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 4;
   for (int base0 = (threadIdx.x & ~31); base0 < total; base0 += kBatch * blockDim.x) {
-    uint2 u[kBatch];
+    uint4 u[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int item = base0 + j * blockDim.x + lane;
-      u[j] = make_uint2(0u, 0u);
+      u[j] = make_uint4(0u, 0u, 0u, 0u);
       if (item < total) {
-        const int m = item / quads, q = item - m * quads;
-        u[j] = ld_cg(reinterpret_cast<const uint2*>(src + (size_t)s_src[m] * K + kc0 + 4 * q));
+        const int m = item / octs, o = item - m * octs;
+        u[j] = ld_cg(reinterpret_cast<const uint4*>(src + (size_t)s_src[m] * K + kc0 + 8 * o));
       }
     }
 #pragma unroll
@@ -308,12 +322,13 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
       if (base >= total) break;
       const int item = base + lane;
       const bool active = item < total;
-      const int m = active ? item / quads : 0;
-      const int q = active ? item - m * quads : 0;
-      const float v[4] = {bf16_to_f32(u[j].x & 0xFFFFu), bf16_to_f32(u[j].x >> 16), bf16_to_f32(u[j].y & 0xFFFFu),
-                          bf16_to_f32(u[j].y >> 16)};
-      quantize_quad_store(v, active, lane, packed + (size_t)(rb.row0 + m) * (K / 2) + (kc0 + 4 * q) / 2,
-                          st.word(m, (kc0 + 4 * q) / 16));
+      const int m = active ? item / octs : 0;
+      const int o = active ? item - m * octs : 0;
+      const float v[8] = {bf16_to_f32(u[j].x & 0xFFFFu), bf16_to_f32(u[j].x >> 16), bf16_to_f32(u[j].y & 0xFFFFu),
+                          bf16_to_f32(u[j].y >> 16),    bf16_to_f32(u[j].z & 0xFFFFu), bf16_to_f32(u[j].z >> 16),
+                          bf16_to_f32(u[j].w & 0xFFFFu), bf16_to_f32(u[j].w >> 16)};
+      quantize_oct_store(v, active, lane, packed + (size_t)(rb.row0 + m) * (K / 2) + (kc0 + 8 * o) / 2,
+                         st.word(m, (kc0 + 8 * o) / 16));
     }
   }
   st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
@@ -334,10 +349,16 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
                                                                         int k, int K, uint8_t* __restrict__ packed,
                                                                         uint8_t* __restrict__ sf) {
   pdl_wait();  // the previous kernel in the stream may still be running
-  pdl_trigger();
   const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
-  if (lead)
+  if (lead) {
+    // The next kernel (the GEMM launch) claims work from these counters as
+    // soon as it starts, before it waits for this kernel: they are cleared,
+    // and the stores performed GPU-wide, before this CTA lets it launch.
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+    __threadfence();
+    __syncthreads();
+  }
+  pdl_trigger();
   __shared__ int s_src[32], s_chunk[32], s_m[32], s_cnt[32], s_R;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -376,6 +397,7 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
           g.group_sf_block[gless] = gless;
           g.group_chunk[gless] = gless;
           reinterpret_cast<int4*>(g.chunk_info)[gless] = make_int4(less, n, e, gless);
+          reinterpret_cast<int4*>(g.block_info)[gless] = make_int4(less, n, e, gless);
         }
       }
     } else if (in && lead) {
@@ -632,7 +654,7 @@ cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_
 
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K, const moe_groups_t& g,
                             int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
-  const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kColsPerCta - 1) / kColsPerCta);
+  const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kQuantCols - 1) / kQuantCols);
   return launch_pdl(quantize_kernel, grid, dim3(kThreads), 0, s, src, src_k, K, g, layout, packed, sf);
 }
 

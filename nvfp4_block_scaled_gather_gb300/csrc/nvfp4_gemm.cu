@@ -8,15 +8,19 @@
 // kernel with 128-row token tiles; this kernel is written for GB300 instead:
 //
 //  * Swap-AB. The weight tile is the MMA's A operand (M = 128 output features)
-//    and the group's tokens are the B operand (N = Mg rounded up to 16, at
-//    most 32 per unit), so a decode group of one row costs a 16-wide MMA, not
+//    and the group's tokens are the B operand (N = the token block's rows
+//    rounded up to 16), so a decode group of one row costs a 16-wide MMA, not
 //    a 128-row tile. The second page ("Tiles below M=8") notes that the wasted
 //    token extent costs no HBM traffic; here it costs no tensor work either.
-//  * Persistent CTAs, two per SM, walk the ragged work list of
-//    (32-token chunk of a group, 128-row weight tile) units in a fixed order;
-//    every unit streams its weight tile over the full K once. Two CTAs per SM
-//    because a CTA's tcgen05 operations execute one after another: with one
-//    CTA per SM the tensor pipe, not HBM, set the pace.
+//  * Persistent CTAs, two per SM, walk the ragged work list of (token block
+//    of a group, 128-row weight tile) units in a fixed order; every unit
+//    streams its weight tile over the full K once. Two CTAs per SM because a
+//    CTA's tcgen05 operations execute one after another: with one CTA per SM
+//    the tensor pipe, not HBM, set the pace (at decode, and at prefill-sized
+//    batches even with a ring twice as deep). Token blocks are 32 rows
+//    (decode and mid-sized batches: more, smaller units) or 128 rows
+//    (prefill-sized batches: each weight tile streams once per 128 rows of a
+//    group, N up to 128 MMAs).
 //  * Weights arrive pre-tiled (nvfp4_tile_weights, a load-time step): for
 //    every 128-row tile and 256-value K stage, 16 KB of e2m1 bytes already in
 //    the 128-byte-swizzled shared-memory image followed by the 2 KB of e4m3
@@ -56,14 +60,17 @@ constexpr int kAtomBytes = 512;     // one scale atom: 128 rows x 4 scales (64 K
 constexpr int kATileBytes = kBM * kStageKBytes;  // 16 KB
 constexpr int kSfStageBytes = 4 * kAtomBytes;    // 2 KB per operand and stage
 constexpr int kWStageBytes = kATileBytes + kSfStageBytes;  // one tiled weight stage: 18 KB
-constexpr int kTokChunk = 32;       // token rows per unit (MMA N <= 32)
+constexpr int kTokChunk = 32;       // epilogue columns per pass (and the small batches' token block)
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 288;       // warp 0: weights, 1: MMA, 2-5: epilogue, 6-7: scale copies, 8: tokens
+// Per CTA, with two CTAs per SM: shared memory (half the SM's 228 KB less
+// 1 KB reserved per CTA) and tensor memory columns (half of the SM's 512).
 constexpr int kCtasPerSm = 2;
-constexpr int kSmemBytes = 114688;  // per CTA: two CTAs fit the SM's 228 KB (1 KB reserved each)
-constexpr int kTmemCols = 256;      // per CTA: half of the SM's 512 columns
-constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: up values [64][33] floats
-constexpr int kXchBytes = 9216;                    // 64 * 33 * 4 rounded up to 1 KB
+constexpr int kSmemBytes = 114688;
+constexpr int kTmemCols = 256;
+constexpr int kXchStride = kTokChunk + 1;          // fused epilogue: gate and up values [2][64][33] floats
+constexpr int kXchHalf = 64 * kXchStride;          // floats of one half (gate or up)
+constexpr int kXchBytes = 17408;                   // 2 * 64 * 33 * 4 rounded up to 1 KB
 constexpr int kUq = 8;                             // unit queue: producer -> MMA, scale copies, epilogue
 constexpr int kHeader = 2048;                      // barriers, TMEM address, queue, small-batch routing tables
 constexpr int kSmallSlots = 32;                    // inline routing: at most 32 slots
@@ -100,8 +107,8 @@ struct GemmArgs {
   const int32_t* topk_ids;  // [S] slots
   int S, E;
   const int32_t* counts;
-  const int32_t* group_chunk;
-  const int32_t* chunk_info;
+  const int4* blk_tab;      // per token block: first row, rows, expert, group
+  int bt;                   // token block rows: 32 (chunk_info) or 128 (block_info)
   int* status;
   int early;                // 1: group metadata and weights were written two or more launches back
   long long wait_budget;    // clock64 cycles a single wait may take
@@ -156,9 +163,6 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -233,6 +237,34 @@ __device__ __forceinline__ uint32_t idesc_nvf4(int n) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
+// h = silu(gate) * up for the globals-scaled halves, in fp32 with CUDA's
+// expf, rounded once to bf16 (returned as the fp32 value of that bf16).
+__device__ __forceinline__ float swiglu_bf16(float gt, float uv) {
+  const float hv = gt / (1.0f + expf(-gt)) * uv;
+  return bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));
+}
+
+// NVFP4 codec across a warp holding one value per lane: lanes 16 b .. 16 b +
+// 15 are one 16-value block (b = 0, 1). Returns, in every lane, the 32-bit
+// word of packed codes of its 8-lane group (lane 8 i + j's code in nibble j)
+// and, in `scales`, the two blocks' e4m3 scale bytes (block 0 low byte).
+__device__ __forceinline__ void quantize_feature(float v, int lane, uint32_t& word, uint32_t& scales) {
+  float amax = fabsf(v);
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
+  const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
+  const float dsc = e4m3_decode(sc);
+  const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
+  uint32_t w = code << (4 * (lane & 7));
+  w |= __shfl_xor_sync(~0u, w, 1);
+  w |= __shfl_xor_sync(~0u, w, 2);
+  w |= __shfl_xor_sync(~0u, w, 4);
+  word = w;
+  scales = sc | (__shfl_sync(~0u, sc, 16) << 8);
+}
+
 struct Ctl {
   volatile int* abort_flag;
   int* status;
@@ -295,9 +327,9 @@ __device__ __noinline__ int ready_stages(const int* ctr, int ks, int nk, int kc4
 
 
 
-// One unit of work: 32-row chunk `chunk` of a group against 128-row weight
-// tile `nt` of the group's expert, for job 0 (units [0, U0)) or job 1. The
-// chunk's token scales are one 512-byte block per K-atom (MOE_SF_CHUNK32).
+// One unit of work: token block `chunk` of a group (32 or 128 rows) against
+// 128-row weight tile `nt` of the group's expert, for job 0 (units [0, U0))
+// or job 1. The block's token scales are one 512-byte atom per 64 K values.
 struct Unit {
   int job, chunk, row0, nvalid, nmma, nt, expert, nk, kc4;
   const uint8_t* w;    // the tile's first 18 KB stage
@@ -312,7 +344,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& p, int U0, in
   un.chunk = v / ntl;
   un.nt = v - un.chunk * ntl;
   // row0, rows, expert, group: the small mode's table in shared memory, else the group metadata
-  const int4 c = tab ? tab[un.chunk] : ld_cg(reinterpret_cast<const int4*>(p.chunk_info) + un.chunk);
+  const int4 c = tab ? tab[un.chunk] : ld_cg(p.blk_tab + un.chunk);
   un.row0 = c.x;
   un.nvalid = c.y;
   un.expert = c.z;
@@ -355,8 +387,9 @@ __device__ __noinline__ void small_route(const GemmArgs& p, int lane, int4* s_ta
   }
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    gemm_kernel(GemmArgs p) {
+// Two CTAs per SM must fit: the register budget ptxas derives from that is
+// 96 a thread (at 108 only one CTA per SM was resident, measured).
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemm_kernel(GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -400,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mbar_init(drain2_bar, 1);
     mbar_init(drain3_bar, 1);
     mbar_init(udone_bar, 4 * 32);
-    mbar_init(xfull_bar, 64);
-    mbar_init(xfree_bar, 64);
+    mbar_init(xfull_bar, 128);  // every epilogue thread stored its row's values
+    mbar_init(xfree_bar, 128);  // every epilogue thread finished reading them
     for (int i = 0; i < kUq; ++i) {
       mbar_init(uqf_bar(i), 1);
       mbar_init(uqe_bar(i), kUqReaders);
@@ -423,8 +456,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const Ctl ctl{abort_flag, p.status, p.wait_budget};
   // Programmatic dependent launch: this grid may start while the previous
   // kernel in the stream still runs. Everything it reads must be complete
-  // first; with p.early the group metadata and the weights are two or more
-  // launches old (complete), and only the token operand waits below.
+  // first. With p.early the group metadata, the work counters and the
+  // weights are two or more launches old (complete); in small mode the
+  // routing is done here from topk_ids (two or more launches old) and the
+  // previous kernel cleared the counters before it let this grid launch. In
+  // both, only the token operand (and whatever follows from it) waits below,
+  // and the first unit's weights stream in meanwhile.
+  const bool early_issue = p.early || p.small;
   if (p.small) {
     // Route the <= 32 slots in warp 0 of every CTA (one slot per lane).
     if (warp == 0) small_route(p, lane, s_tab, s_meta);
@@ -437,34 +475,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // ---- schedule shape, identical on every thread ----
   const int G = p.small ? s_meta[0] : ld_cg(p.counts + 0);
   const int maxmg = p.small ? s_meta[2] : ld_cg(p.counts + 2);
-  const int nchunks = p.small ? G : (G > 0 ? ld_cg(p.group_chunk + G) : 0);
+  const int nchunks = p.small ? G : ld_cg(p.counts + (p.bt == 128 ? 3 : 4));  // token blocks
   const int nt0 = p.j0.N / kBM;
   const int nt1 = p.njobs > 1 ? p.j1.N / kBM : 1;
   const int U0 = nchunks * nt0;
   const int total_units = U0 + (p.njobs > 1 ? nchunks * nt1 : 0);
   const int nk1 = p.njobs > 1 ? (p.j1.K + 255) / 256 : 1;  // job-1 K stages (dependency counters per chunk)
   const bool has_xch = p.fused0 != 0;
-  const int tn = min(kTokChunk, max(16, (maxmg + 15) & ~15));   // token rows per B stage
-  const int acc_cols = max(32, tn);
+  const int tn = min(p.bt, max(16, (maxmg + 15) & ~15));   // token rows per B stage (MMA N at most)
+  const int acc_cols = (tn + 31) & ~31;                     // accumulator buffers start 32-column aligned
+  const int nacc = 2 * acc_cols + 64 <= kTmemCols ? 2 : 1;  // double-buffered unless TMEM is short
   const int stage_bytes = kWStageBytes + tn * kStageKBytes + kSfStageBytes;
   const int avail = kSmemBytes - 1024 - kHeader - (has_xch ? kXchBytes : 0);
   int stages = min(kMaxStages, avail / stage_bytes);
-  stages = min(stages, (kTmemCols - 2 * acc_cols) / 32);
+  stages = min(stages, (kTmemCols - nacc * acc_cols) / 32);
   // per stage: [weights 16 KB | weight scales 2 KB] ... then token rows, token scales, exchange
   const uint32_t sW = smem_u32(smem + kHeader);
   const uint32_t sB = sW + (uint32_t)stages * kWStageBytes;
   const uint32_t sSFB = sB + (uint32_t)stages * tn * kStageKBytes;
-  if (p.small) {
-    // the first claims hand out units 0 .. gridDim.x - 1: warm L2 with this
-    // CTA's share of their first stages while the rows are still being quantized
-    if (threadIdx.x == 0 && (int)blockIdx.x < total_units) {
-      const Unit un = decode_unit(blockIdx.x, p, U0, nt0, nt1, tab);
-      for (int ks = 0; ks < un.nk && ks < stages; ++ks)
-        prefetch_l2(un.w + (size_t)ks * kWStageBytes, kATileBytes + min(4, un.kc4 - 4 * ks) * kAtomBytes);
-    }
-    pdl_wait();
-    pdl_trigger();
-  }
   float* xch = reinterpret_cast<float*>(smem + kHeader + (size_t)stages * stage_bytes);
 
 
@@ -516,11 +544,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       const uint64_t stream_policy = policy_evict_first();
-      // With p.early, the first unit's first weight stages go out before
+      // With early_issue, the first unit's first weight stages go out before
       // waiting for the previous kernel (they do not depend on it).
       int cur = (total_units > 0) ? claim() : -1;
       int prefetched = 0;
-      if (p.early) {
+      if (early_issue) {
         if (cur >= 0) {
           const Unit un = decode_unit(cur, p, U0, nt0, nt1, tab);
           for (int ks = 0; ks < un.nk && ks < stages; ++ks) {
@@ -581,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // written by job 0: the copies of its K stage ks wait until the job-0
     // tiles that write those h features are done (the weights stream on
     // meanwhile).
-    if (p.early) pdl_wait();  // the token rows come from the previous kernel
+    if (early_issue) pdl_wait();  // the token rows come from the previous kernel
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -609,9 +637,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t dst = sB + (uint32_t)(stage * tn * kStageKBytes);
         const int per_row = 2 * natoms;
         const uint8_t* src = rows + (size_t)ks * kStageKBytes;
-        for (int i = lane; i < un.nvalid * per_row; i += 32) {
-          const int r = i / per_row, c = i - r * per_row;
-          cp_async16(dst + (uint32_t)(r * kStageKBytes + ((c ^ (r & 7)) << 4)), src + (size_t)r * (K / 2) + c * 16);
+        if (per_row == 8) {  // a full stage: 8 pieces per row (shifts, not a division)
+          for (int i = lane; i < un.nvalid * 8; i += 32) {
+            const int r = i >> 3, c = i & 7;
+            cp_async16(dst + (uint32_t)(r * kStageKBytes + ((c ^ (r & 7)) << 4)), src + (size_t)r * (K / 2) + c * 16);
+          }
+        } else {
+          for (int i = lane; i < un.nvalid * per_row; i += 32) {
+            const int r = i / per_row, c = i - r * per_row;
+            cp_async16(dst + (uint32_t)(r * kStageKBytes + ((c ^ (r & 7)) << 4)), src + (size_t)r * (K / 2) + c * 16);
+          }
         }
         const uint32_t sdst = sSFB + (uint32_t)(stage * kSfStageBytes);
         const uint8_t* ssrc = un.sfb + (size_t)ks * kSfStageBytes;
@@ -643,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           tc_fence_after();
           if (tok) fence_proxy_async_shared();  // token scales were written by cp.async
           const int natoms = min(4, kc4 - 4 * ks);
-          const uint32_t col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage + (tok ? 16 : 0));
+          const uint32_t col = tmem_base + (uint32_t)(nacc * acc_cols + 32 * stage + (tok ? 16 : 0));
           const uint64_t src = desc_scales(tok ? sSFB + stage * kSfStageBytes : sW + stage * kWStageBytes + kATileBytes);
           // atom a at +512 bytes: +32 in the descriptor's address field
           for (int a = 0; a < natoms; ++a) tc_cp_scales(col + 4 * a, src + 32 * a);
@@ -684,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           tc_fence_after();
           fence_proxy_async_shared();  // the token rows were written by cp.async
           const int natoms = min(4, un.kc4 - 4 * ks);
-          const uint32_t sf_col = tmem_base + (uint32_t)(2 * acc_cols + 32 * stage);
+          const uint32_t sf_col = tmem_base + (uint32_t)(nacc * acc_cols + 32 * stage);
           // K step a (32 bytes along the 128-byte swizzled rows): +2 in the address field
           const uint64_t adesc = desc_sw128(sW + stage * kWStageBytes);
           const uint64_t bdesc = desc_sw128(sB + stage * tn * kStageKBytes);
@@ -703,8 +738,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         if (!ok) break;
         tc_commit(accf_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok || *abort_flag) {  // this role, or another, gave up: nothing of ours may be in flight at exit
         // wait for every MMA issued so far before TMEM is freed
@@ -716,85 +750,100 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   } else {
     // ============================== epilogue ==============================
+    // The unit's accumulator (tile rows = TMEM lanes, token rows = columns)
+    // is read 32 columns at a time; the buffer is released after the last
+    // read. Plain: fp32 rows of d. Fused (job 0 of the layer): SwiGLU with
+    // the per-half globals, bf16 rounding and the NVFP4 codec, written as h.
     const int quad = warp & 3;     // TMEM lanes 32*quad .. 32*quad+31 = tile rows
     const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    const int tr = quad * 32 + lane;  // tile row
     const int half = p.j0.N / 2;
     int acc = 0;
     uint32_t acc_phase = 0, xph = 0, uph = 0;
-    while (true) {
+    bool ok = true;
+    while (ok) {
       const int u = next_unit();
       if (u < 0) break;
       const Unit un = decode_unit(u, p, U0, nt0, nt1, tab);
       if (!wait_phase(accf_bar(acc), acc_phase, ctl)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * acc_cols);
-      uint32_t r[kTokChunk];
-      // one load of 16 or 32 columns from the buffer's first column (aligned)
-      if (un.nvalid <= 16) {
-        tc_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
-      } else {
-        tc_ld_32x32b_x32(taddr, r);
-      }
-      tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(acce_bar(acc));  // the accumulator buffer is free again
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-      const int tr = quad * 32 + lane;  // tile row
-      if (un.job == 1 || !p.fused0) {
-        const int N = un.job ? p.j1.N : p.j0.N;
-        const int il = un.job ? p.j1.interleaved : p.j0.interleaved;
-        const int n = !il ? un.nt * kBM + tr : (tr < 64 ? un.nt * 64 + tr : N / 2 + un.nt * 64 + (tr - 64));
-        float* dst = (un.job ? p.j1.d : p.j0.d) + (size_t)un.row0 * N + n;
-#pragma unroll
-        for (int j = 0; j < kTokChunk; ++j)
-          if (j < un.nvalid) dst[(size_t)j * N] = __uint_as_float(r[j]);
-      } else {
-        // ---- fused SwiGLU + requantize: up rows (lanes 64..127) to smem, gate rows compute ----
-        uint8_t* sfblk = p.h_sf + ((size_t)un.chunk * (half / 64) + un.nt) * kAtomBytes;  // atom nt of the chunk
-        if (quad >= 2) {
-          if (!wait_phase(xfree_bar, xph ^ 1u, ctl)) break;
-          const int f = tr - 64;
+      const bool fused = un.job == 0 && p.fused0;
+      // plain: this thread's output column n of d, rows row0 ..
+      const int N = un.job ? p.j1.N : p.j0.N;
+      const int il = un.job ? p.j1.interleaved : p.j0.interleaved;
+      const int n = !il ? un.nt * kBM + tr : (tr < 64 ? un.nt * 64 + tr : N / 2 + un.nt * 64 + (tr - 64));
+      float* dst = fused ? nullptr : (un.job ? p.j1.d : p.j0.d) + (size_t)un.row0 * N + n;
+      // fused: atom nt of the block's h scales (h features 64 nt .. 64 nt + 63) and this thread's h bytes
+      uint8_t* sfblk = fused ? p.h_sf + ((size_t)un.chunk * (half / 64) + un.nt) * kAtomBytes : nullptr;
+      const float gg = fused ? ld_cg(p.g_gate_up + 2 * un.expert) : 0.0f;
+      const float gu = fused ? ld_cg(p.g_gate_up + 2 * un.expert + 1) : 0.0f;
+      uint8_t* hp_base = fused ? p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 : nullptr;
+      for (int c0 = 0; c0 < un.nvalid; c0 += kTokChunk) {
+        const int nc = min(kTokChunk, un.nvalid - c0);  // uniform across the warp
+        uint32_t r[kTokChunk];
+        // 16 or 32 columns from a 32-column-aligned address
+        if (nc <= 16) {
+          tc_ld_32x32b_x16(taddr + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(r));
+        } else {
+          tc_ld_32x32b_x32(taddr + (uint32_t)c0, r);
+        }
+        tc_wait_ld();
+        if (c0 + kTokChunk >= un.nvalid) {
+          tc_fence_before();
+          mbar_arrive(acce_bar(acc));  // the accumulator buffer is free again
+        }
+        if (!fused) {
 #pragma unroll
           for (int j = 0; j < kTokChunk; ++j)
-            if (j < un.nvalid) xch[f * kXchStride + j] = __uint_as_float(r[j]);
-          mbar_arrive(xfull_bar);
-        } else {
-          if (!wait_phase(xfull_bar, xph, ctl)) break;
-          const float gg = ld_cg(p.g_gate_up + 2 * un.expert), gu = ld_cg(p.g_gate_up + 2 * un.expert + 1);
-          uint8_t* hp = p.h_packed + (size_t)un.row0 * (half / 2) + un.nt * 32 + quad * 16 + (lane >> 1);
-#pragma unroll
-          for (int j = 0; j < kTokChunk; ++j) {
-            if (j >= un.nvalid) break;  // uniform across the warp
-            const float gt = __uint_as_float(r[j]) * gg;
-            const float uv = xch[tr * kXchStride + j] * gu;
-            const float hv = gt / (1.0f + expf(-gt)) * uv;
-            const float v = bf16_to_f32(__bfloat16_as_ushort(__float2bfloat16_rn(hv)));  // h rounded once to bf16
-            float amax = fabsf(v);  // 16-feature block = 16 lanes
-            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
-            amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
-            const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
-            const float dsc = e4m3_decode(sc);
-            const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
-            uint32_t w = code << (4 * (lane & 7));  // 8 features -> one 32-bit word, feature 2i low nibble
-            w |= __shfl_xor_sync(~0u, w, 1);
-            w |= __shfl_xor_sync(~0u, w, 2);
-            w |= __shfl_xor_sync(~0u, w, 4);
-            const uint32_t sc_hi = __shfl_sync(~0u, sc, 16);
-            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(hp + (size_t)j * (half / 2)) = w;
-            if (lane == 0) *reinterpret_cast<uint16_t*>(sfblk + j * 16 + 2 * quad) = (uint16_t)(sc | (sc_hi << 8));
-          }
-          mbar_arrive(xfree_bar);
+            if (j < nc) dst[(size_t)(c0 + j) * N] = __uint_as_float(r[j]);
+          continue;
         }
+        // ---- fused SwiGLU + requantize ----
+        // Every epilogue thread stores its row's values (gate rows: tile rows
+        // 0..63, up rows: 64..127, feature = row % 64) to shared memory; then
+        // warp q computes features 32 (q % 2) .. + 31 for every other column
+        // (columns q / 2, q / 2 + 2, ...): all four warps share the per-column
+        // chain (SwiGLU, block amax, codec), which with only the two gate-row
+        // warps working made the epilogue, not the MMAs, pace 48-row blocks.
+        if (!wait_phase(xfree_bar, xph ^ 1u, ctl)) { ok = false; break; }
+        {
+          float* row = xch + (quad >= 2 ? kXchHalf : 0) + (tr & 63) * kXchStride;
+#pragma unroll
+          for (int j = 0; j < kTokChunk; ++j)
+            if (j < nc) row[j] = __uint_as_float(r[j]);
+        }
+        mbar_arrive(xfull_bar);
+        if (!wait_phase(xfull_bar, xph, ctl)) { ok = false; break; }
+        {
+          const int f = (quad & 1) * 32 + lane;  // feature 64 nt + f of h
+          const float* grow = xch + f * kXchStride;
+          const float* urow = xch + kXchHalf + f * kXchStride;
+          uint8_t* hpf = hp_base + (quad & 1) * 16 + (lane >> 1);
+          uint8_t* sfq = sfblk + 2 * (quad & 1);
+          for (int j0 = quad >> 1; j0 < nc; j0 += 2) {
+            const float h0 = swiglu_bf16(grow[j0] * gg, urow[j0] * gu);
+            uint32_t w0, s0;
+            quantize_feature(h0, lane, w0, s0);
+            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(hpf + (size_t)(c0 + j0) * (half / 2)) = w0;
+            if (lane == 0) {
+              const int m0 = c0 + j0;
+              *reinterpret_cast<uint16_t*>(sfq + (m0 & 31) * 16 + (m0 >> 5) * 4) = (uint16_t)s0;
+            }
+          }
+        }
+        mbar_arrive(xfree_bar);
         xph ^= 1u;
-        // the rest of the chunk's 512-byte scale block (other words, rows past the chunk) is zero
-        const int row = et >> 2, wi = et & 3;
-        if (wi != 0 || row >= un.nvalid) reinterpret_cast<uint32_t*>(sfblk)[et] = 0u;
+      }
+      if (!ok) break;
+      if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
+      if (fused) {
+        // the rest of the block's 512-byte scale atom (token rows past the block's rows) is zero:
+        // word et holds row (et / 4) + 32 (et % 4)
+        if ((et >> 2) + 32 * (et & 3) >= un.nvalid) reinterpret_cast<uint32_t*>(sfblk)[et] = 0u;
       }
       if (un.job == 0 && p.njobs > 1) {
-        // publish this tile of the chunk to job 1: the writers' arrivals
+        // publish this tile of the block to job 1: the writers' arrivals
         // (release, CTA scope) reach one thread, whose release-add at GPU
         // scope makes all of them visible to the acquiring reader
         mbar_arrive(udone_bar);
@@ -827,10 +876,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const GemmJob& j0, const SwigluOut* swiglu,
-                                const GemmJob* j1, int* gate, const SmallFront* front, bool early, int* status,
-                                cudaStream_t s) {
-  if (front && (early || front->S > kSmallSlots || front->S < 1)) return cudaErrorInvalidValue;
+cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, int layout, const GemmJob& j0,
+                                const SwigluOut* swiglu, const GemmJob* j1, int* gate, const SmallFront* front,
+                                bool early, int* status, cudaStream_t s) {
+  if (front && (early || front->S > kSmallSlots || front->S < 1 || layout != MOE_SF_CHUNK32))
+    return cudaErrorInvalidValue;
   if (j1 && !gate) return cudaErrorInvalidValue;
   GemmArgs p = {};
   auto fill = [](Job& J, const GemmJob& src) {
@@ -855,8 +905,9 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
   p.exit_ctr = j1 ? gate + 1 : nullptr;
   p.chunk_done = j1 ? gate + 2 : nullptr;
   p.counts = g.counts;
-  p.group_chunk = g.group_chunk;
-  p.chunk_info = g.chunk_info;
+  const bool big = layout == MOE_SF_ATOM128;
+  p.bt = big ? 128 : kTokChunk;
+  p.blk_tab = reinterpret_cast<const int4*>(big ? g.block_info : g.chunk_info);
   p.status = status;
   p.early = early ? 1 : 0;
   if (front) {
@@ -866,12 +917,12 @@ cudaError_t launch_grouped_gemm(const moe_groups_t& g, int R_max, int E, const G
     p.E = E;
   }
   p.wait_budget = 2000000000LL;
+  const long long units_bound = row_blocks_bound(R_max, E, layout) * (j0.N / kBM + (j1 ? j1->N / kBM : 0));
   cudaError_t err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  const long long units_bound = chunks_bound(R_max, E) * (j0.N / kBM + (j1 ? j1->N / kBM : 0));
   const long long slots = (long long)num_sms() * kCtasPerSm;
   const int grid = (int)(units_bound < slots ? units_bound : slots);
   return launch_pdl(gemm_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), kSmemBytes, s, p);

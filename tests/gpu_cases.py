@@ -241,6 +241,11 @@ def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
     info = [(ref_offs[g] + 32 * q, min(32, ref_offs[g + 1] - ref_offs[g] - 32 * q), ref_gexp[g], g)
             for g in range(G) for q in range(chunks[g + 1] - chunks[g])]
     assert np.array_equal(host["chunk_info"].numpy(), np.array(info, dtype=np.int64).reshape(-1, 4))
+    blocks = O.group_sf_blocks(ref_offs)
+    binfo = [(ref_offs[g] + 128 * q, min(128, ref_offs[g + 1] - ref_offs[g] - 128 * q), ref_gexp[g], g)
+             for g in range(G) for q in range(blocks[g + 1] - blocks[g])]
+    assert np.array_equal(host["block_info"].numpy(), np.array(binfo, dtype=np.int64).reshape(-1, 4))
+    assert host["blocks"] == blocks[-1]
     assert host["max_mg"] == (int(np.diff(ref_offs).max()) if G else 0)
     slot_row = np.full(S, -1)
     slot_row[ref_row_slot] = np.arange(len(ref_row_slot))

@@ -53,13 +53,16 @@ def test_host_side_validation(native):
     g = _fake_groups()
     s = None
     # unsupported GEMM shapes
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 0, 4, 100, 256, 16, s) == 2
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 0, 4, 128, 96, 16, s) == 2
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 16, 1, 4, 384, 256, 16, s) == 2
-    assert native.nvfp4_grouped_gemm_swiglu(16, 16, ctypes.byref(g), 8, 16, 4, 192, 256, 16, 16, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, 1, ctypes.byref(g), 8, 16, 0, 4, 100, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, 1, ctypes.byref(g), 8, 16, 0, 4, 128, 96, 16, s) == 2
+    assert native.nvfp4_grouped_gemm(16, 16, 1, ctypes.byref(g), 8, 16, 1, 4, 384, 256, 16, s) == 2
+    assert native.nvfp4_grouped_gemm_swiglu(16, 16, 1, ctypes.byref(g), 8, 16, 4, 192, 256, 16, 16, 16, s) == 2
+    # token-scale layout must be one of the two
+    assert native.nvfp4_grouped_gemm(16, 16, 2, ctypes.byref(g), 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm_swiglu(16, 16, -1, ctypes.byref(g), 8, 16, 4, 128, 256, 16, 16, 16, s) == 1
     # missing group arrays / bad sizes / misaligned weights
-    assert native.nvfp4_grouped_gemm(16, 16, None, 8, 16, 0, 4, 128, 256, 16, s) == 1
-    assert native.nvfp4_grouped_gemm(16, 16, ctypes.byref(g), 8, 24, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm(16, 16, 1, None, 8, 16, 0, 4, 128, 256, 16, s) == 1
+    assert native.nvfp4_grouped_gemm(16, 16, 1, ctypes.byref(g), 8, 24, 0, 4, 128, 256, 16, s) == 1
     assert native.nvfp4_quantize_rows(16, 8, 100, 4, ctypes.byref(g), 1, 16, 16, s) == 2
     assert native.nvfp4_quantize_rows(16, 8, 128, 0, ctypes.byref(g), 1, 16, 16, s) == 1
     assert native.nvfp4_quantize_rows(16, 8, 128, 4, ctypes.byref(g), 7, 16, 16, s) == 1
@@ -131,3 +134,16 @@ def test_groups_carve_is_host_only(native):
     assert native.moe_groups_carve(base, 3, 2, 5, ctypes.byref(g)) == 0
     assert g.counts == base and g.slot_row > g.row_slot > g.group_offsets
     assert native.moe_groups_carve(base + 4, 3, 2, 5, ctypes.byref(g)) == 1
+
+
+def test_layer_token_block_rule(native):
+    """The layer's token blocks: 32-row chunks for decode-sized and mid-sized
+    batches, 128-row blocks once the batch routes 16 rows per expert on
+    average (T*k >= 16*E), never for the one-launch decode front end."""
+    assert native.moe_nvfp4_layer_sf_layout(1, 8, 288) == 1
+    assert native.moe_nvfp4_layer_sf_layout(32, 8, 288) == 1
+    assert native.moe_nvfp4_layer_sf_layout(288, 8, 288) == 1         # ~2300 rows, mean 8 per expert
+    assert native.moe_nvfp4_layer_sf_layout(576, 8, 288) == 0         # mean 16 per expert
+    assert native.moe_nvfp4_layer_sf_layout(1152, 8, 288) == 0        # prefill-sized, mean 32
+    assert native.moe_nvfp4_layer_sf_layout(4, 8, 1) == 1             # decode front end (T*k <= 32)
+    assert native.moe_nvfp4_layer_sf_layout(160, 2, 6) == 0

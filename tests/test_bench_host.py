@@ -24,18 +24,28 @@ def _run_bench(args, env_extra=None, timeout=300):
 
 
 def test_reference_arm_prints_the_contract_line():
-    r = _run_bench(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1",
-                    "--cpu-seconds", "1"])
+    r = _run_bench(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1"])
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
     assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] >= 1 and d["higher_is_better"] is True
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == bench.host_cores()
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("tiny")
+
+
+def test_cpu_baseline_reports_all_cores_and_one():
+    """The oracle timed on every host core (one spawned process each) and on
+    one, over whole steps of the config's first token."""
+    d = bench.cpu_baseline("tiny")
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cores"] == bench.host_cores()
+    one = d["single_core"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["kind"] == "oracle"
+    assert "top-2" in d["sample"] and "spawned" in d["sample"]
 
 
 def test_reference_arm_runs_on_rank_0_only():

@@ -74,6 +74,11 @@ def test_grouped_gemm_edge_scales(cuda, mg, N_, K):
     want_sf = chunk32_bytes(scales, offs, K)
     assert np.array_equal(xsf[:want_sf.size].cpu().numpy(), want_sf)
     ref = O.grouped_gemm(xq_ref, xsf_ref, offs, gexp, packed.numpy(), sfl.numpy())
+    # the same rows in 128-row token blocks (the pages' ATOM128 scale layout)
+    xq_a = torch.zeros_like(xq)
+    xsf_a = torch.zeros(N.sf_bytes(R, E, K, N.SF_ATOM128), dtype=torch.uint8, device=cuda)
+    N.nvfp4_quantize_rows(np_to_bf16(rows, cuda), G, xq_a, xsf_a, N.SF_ATOM128)
+    assert torch.equal(xq_a, xq) and np.array_equal(xsf_a[:xsf_ref.size].cpu().numpy(), xsf_ref)
     for interleave in ((False, True) if N_ % 256 == 0 else (False,)):
         tw = N.TiledWeight(packed.to(cuda), sfl.to(cuda), interleave=interleave)
         d = torch.full((R, N_), 7.0, dtype=torch.float32, device=cuda)
@@ -81,6 +86,9 @@ def test_grouped_gemm_edge_scales(cuda, mg, N_, K):
         got = d.cpu().numpy()
         assert rel_fro(got, ref) <= GEMM_TOL, interleave
         assert _rowwise_rel(got, ref) <= GEMM_TOL, interleave
+        d_a = torch.full((R, N_), 7.0, dtype=torch.float32, device=cuda)
+        N.nvfp4_grouped_gemm(xq_a, xsf_a, G, tw, d_a, layout=N.SF_ATOM128)
+        assert torch.equal(d_a, d), interleave
     assert N.check_status() == 0
 
 

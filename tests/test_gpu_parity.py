@@ -326,6 +326,48 @@ def test_expert_gemms_one_launch_equals_two(small):
     assert N.check_status() == 0
 
 
+def test_128_row_token_blocks_equal_32_row_chunks(small):
+    """The same GEMMs over 128-row token blocks (MOE_SF_ATOM128 scales: one
+    unit per weight tile for the 140-row group's first 128 rows, MMA N = 128)
+    give the bits of the 32-row chunks: plain w13 and w2, the fused SwiGLU
+    epilogue (h scales written in the 128-row layout, equal to the quantizer's
+    ATOM128 output), and the one-launch pair of GEMMs."""
+    E, x, ids, tw, W, *_ = small
+    st = run_stages(x, ids, tw, W, E)
+    dev = x.device
+    T, k = ids.shape
+    S, R = T * k, st["groups"]["R"]
+    G = N.Groups(T, k, E, dev)
+    N.moe_route_groups(ids, E, G)
+    A = N.SF_ATOM128
+    xsf = torch.zeros(N.sf_bytes(S, E, W.H, A), dtype=torch.uint8, device=dev)
+    xq = torch.zeros_like(st["xq"])
+    N.nvfp4_quantize_rows(st["xg"], G, xq, xsf, A)
+    hsf_ref = torch.zeros(N.sf_bytes(S, E, W.I, A), dtype=torch.uint8, device=dev)
+    hq_ref = torch.zeros_like(st["hq"])
+    N.nvfp4_quantize_rows(st["h"], G, hq_ref, hsf_ref, A)
+    for _ in range(2):
+        d13 = torch.zeros_like(st["d13"])
+        N.nvfp4_grouped_gemm(xq, xsf, G, W.w13, d13, layout=A)
+        d2 = torch.zeros_like(st["d2"])
+        N.nvfp4_grouped_gemm(hq_ref, hsf_ref, G, W.w2, d2, layout=A)
+        hq, hsf = torch.zeros_like(hq_ref), torch.full_like(hsf_ref, 0xAB)
+        N.nvfp4_grouped_gemm_swiglu(xq, xsf, G, W.w13, W.g_gate_up, hq, hsf, layout=A)
+        torch.cuda.synchronize()
+        assert torch.equal(d13[:R], st["d13"][:R]) and torch.equal(d2[:R], st["d2"][:R])
+        routed = G.host()["blocks"] * 128 * (W.I // 16)   # every byte of the routed blocks' regions
+        assert torch.equal(hq[:R], st["hq"][:R]) and torch.equal(hsf[:routed], hsf_ref[:routed])
+    gate = torch.zeros(N.expert_gemms_gate_bytes(S, E, W.I), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        hq, hsf, d2 = torch.zeros_like(hq_ref), torch.zeros_like(hsf_ref), torch.zeros_like(st["d2"])
+        N.nvfp4_moe_expert_gemms(xq, xsf, G, W, hq, hsf, d2, gate, layout=A)
+        torch.cuda.synchronize()
+        assert torch.equal(hq[:R], st["hq"][:R]) and torch.equal(hsf, hsf_ref)
+        assert torch.equal(d2[:R], st["d2"][:R])
+    assert int(gate.sum()) == 0
+    assert N.check_status() == 0
+
+
 def test_bounded_wait_reports_timeout_and_the_context_survives(small):
     """Failure detection without a fault: start the two-GEMM launch's claim
     counter past every w13 unit, so no chunk's h is ever published and every
@@ -358,20 +400,23 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(small):
 
 def test_back_to_back_calls_share_a_workspace(small):
     """Layer calls queued back to back (no host sync) on one workspace,
-    alternating the one-launch small-batch front end (T*k <= 32) and the
-    general one (route, then gather+quantize): every call's output equals the
-    same call run alone. Kernels start before the one they depend on ends
+    alternating the one-launch small-batch front end (T*k <= 32), the
+    general one (route, then gather+quantize) with 32-row token chunks and
+    with 128-row token blocks (the one-CTA-per-SM GEMM): every call's output
+    equals the same call run alone. Kernels start before the one they depend on ends
     (programmatic dependent launch), so a read of an earlier kernel's output
     that could hit a stale cached line shows up here."""
     E, x, ids, tw, W, *_ = small
-    cases = {n: (x[:n].contiguous(), ids[:n].contiguous(), tw[:n].contiguous()) for n in (3, 40)}
+    cases = {n: (x[:n].contiguous(), ids[:n].contiguous(), tw[:n].contiguous()) for n in (3, 40, 60)}
+    assert N.layer_sf_layout(60, ids.shape[1], E) == N.SF_ATOM128     # 128-row blocks, one CTA per SM
+    assert N.layer_sf_layout(40, ids.shape[1], E) == N.SF_CHUNK32
     refs = {n: N.MoeLayer(W, n, ids.shape[1])(*c).clone() for n, c in cases.items()}
     torch.cuda.synchronize()
-    ws = torch.zeros(N.moe_nvfp4_layer_workspace_size(40, ids.shape[1], E, W.H, W.I), dtype=torch.uint8,
-                     device=x.device)
+    ws = torch.zeros(max(N.moe_nvfp4_layer_workspace_size(n, ids.shape[1], E, W.H, W.I) for n in cases),
+                     dtype=torch.uint8, device=x.device)
     outs = []
     for _ in range(5):
-        for n in (40, 3, 3, 40, 3):
+        for n in (40, 3, 60, 3, 40, 60, 60, 3):
             y = torch.empty_like(cases[n][0])
             N.moe_nvfp4_layer(*cases[n], W, ws, y)
             outs.append((n, y))
