@@ -187,17 +187,6 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
   if ((lane & 15) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
-// e2m1 codes of two fp32 values, round to nearest even, saturating at 6: the
-// hardware conversion (the same rounding as e2m1_encode, sign of zero kept);
-// `lo` goes to the low nibble.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint16_t b;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
-      : "=h"(b)
-      : "f"(hi), "f"(lo));
-  return b;
-}
-
 // Lane pairs (2j, 2j+1) of a warp hold one 16-value block, eight values each;
 // eight lanes hold the four blocks of one 4-byte scale word. Each lane writes
 // its four packed bytes; the first lane of each eight writes the word. Lanes
@@ -205,17 +194,8 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
 // nothing; an 8-lane group is either wholly active or wholly not.
 __device__ __forceinline__ void quantize_oct_store(const float (&v)[8], bool active, int lane,
                                                    uint8_t* __restrict__ packed_dst, uint32_t* __restrict__ word) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
-  const uint32_t s = e4m3_encode(__fdiv_rn(amax, 6.0f));
-  const float d = e4m3_decode(s);
-  uint32_t codes = 0u;
-  if (d != 0.0f) {  // an underflowed block keeps all-zero codes
-#pragma unroll
-    for (int i = 0; i < 4; ++i) codes |= e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d)) << (8 * i);
-  }
+  uint32_t codes, s;
+  quantize_oct(v, codes, s);
   const uint32_t s1 = __shfl_down_sync(~0u, s, 2), s2 = __shfl_down_sync(~0u, s, 4),
                  s3 = __shfl_down_sync(~0u, s, 6);
   if (!active) return;
@@ -324,9 +304,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
       const bool active = item < total;
       const int m = active ? item / octs : 0;
       const int o = active ? item - m * octs : 0;
-      const float v[8] = {bf16_to_f32(u[j].x & 0xFFFFu), bf16_to_f32(u[j].x >> 16), bf16_to_f32(u[j].y & 0xFFFFu),
-                          bf16_to_f32(u[j].y >> 16),    bf16_to_f32(u[j].z & 0xFFFFu), bf16_to_f32(u[j].z >> 16),
-                          bf16_to_f32(u[j].w & 0xFFFFu), bf16_to_f32(u[j].w >> 16)};
+      float v[8];
+      bf16x8_to_f32(u[j], v);
       quantize_oct_store(v, active, lane, packed + (size_t)(rb.row0 + m) * (K / 2) + (kc0 + 8 * o) / 2,
                          st.word(m, (kc0 + 8 * o) / 16));
     }

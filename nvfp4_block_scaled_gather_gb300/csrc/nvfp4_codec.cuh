@@ -76,6 +76,43 @@ __device__ __forceinline__ Nvfp4Block quantize16(const float* v) {
   return out;
 }
 
+// e2m1 codes of two fp32 values, round to nearest even, saturating at 6: the
+// hardware conversion (the same rounding as e2m1_encode, sign of zero kept);
+// `lo` goes to the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t b;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(b)
+      : "f"(hi), "f"(lo));
+  return b;
+}
+
+// NVFP4 codec for eight values per lane, a lane pair (2j, 2j+1) holding one
+// 16-value block: the pair's block scale (e4m3 of amax / 6) and this lane's
+// four packed code bytes (value 2i in the low nibble of byte i). Every lane
+// of the warp must take part (one shuffle).
+__device__ __forceinline__ void quantize_oct(const float (&v)[8], uint32_t& codes, uint32_t& scale) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+  scale = e4m3_encode(__fdiv_rn(amax, 6.0f));
+  const float d = e4m3_decode(scale);
+  codes = 0u;
+  if (d != 0.0f) {  // an underflowed block keeps all-zero codes
+#pragma unroll
+    for (int i = 0; i < 4; ++i) codes |= e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d)) << (8 * i);
+  }
+}
+
+// Eight bf16 values (one 16-byte load) as fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
+  v[0] = bf16_to_f32(u.x & 0xFFFFu); v[1] = bf16_to_f32(u.x >> 16);
+  v[2] = bf16_to_f32(u.y & 0xFFFFu); v[3] = bf16_to_f32(u.y >> 16);
+  v[4] = bf16_to_f32(u.z & 0xFFFFu); v[5] = bf16_to_f32(u.z >> 16);
+  v[6] = bf16_to_f32(u.w & 0xFFFFu); v[7] = bf16_to_f32(u.w >> 16);
+}
+
 // Byte offset of scale (row m, column c) in a region of 128-row atoms with
 // Kc scale columns: atoms run along K, then along rows; inside an atom,
 // 16 bytes per row of a 32-row slab and 4 bytes per 32-row quarter.
