@@ -177,8 +177,9 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
   const float d = e4m3_decode(s);
   uint32_t codes = 0u;
   if (d != 0.0f) {  // an underflowed block keeps all-zero codes
+    const float r = __frcp_rn(d);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) codes |= e2m1_encode(__fdiv_rn(v[i], d)) << (4 * i);
+    for (int i = 0; i < 4; ++i) codes |= e2m1_encode(quotient_for_e2m1(v[i], d, r)) << (4 * i);
   }
   const uint32_t s1 = __shfl_down_sync(~0u, s, 4), s2 = __shfl_down_sync(~0u, s, 8),
                  s3 = __shfl_down_sync(~0u, s, 12);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   __syncthreads();
   // Up to kBatch of this warp's items loaded before any is quantized, so that
   // a block of many rows costs one memory round trip per kBatch, not per row.
-  constexpr int kBatch = 4;
+  constexpr int kBatch = 2;  // 2 in flight: 40 registers, six CTAs of 256 threads per SM
   for (int base0 = (threadIdx.x & ~31); base0 < total; base0 += kBatch * blockDim.x) {
     uint4 u[kBatch];
 #pragma unroll

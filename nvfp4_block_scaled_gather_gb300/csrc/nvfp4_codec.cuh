@@ -53,29 +53,6 @@ __device__ __forceinline__ uint32_t e2m1_encode(float v) {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits) { return __uint_as_float(bits << 16); }
 
-// One 16-element block: scale code and 8 packed bytes (as two u32, element
-// 2j in the low nibble of byte j). `v` holds fp32 values exact in bf16.
-struct Nvfp4Block {
-  uint32_t scale;
-  uint32_t lo, hi;
-};
-
-__device__ __forceinline__ Nvfp4Block quantize16(const float* v) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  Nvfp4Block out;
-  out.scale = e4m3_encode(__fdiv_rn(amax, 6.0f));
-  const float d = e4m3_decode(out.scale);
-  out.lo = out.hi = 0u;
-  if (d == 0.0f) return out;              // underflowed block: all-zero codes
-#pragma unroll
-  for (int i = 0; i < 8; ++i) out.lo |= e2m1_encode(__fdiv_rn(v[i], d)) << (4 * i);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) out.hi |= e2m1_encode(__fdiv_rn(v[8 + i], d)) << (4 * i);
-  return out;
-}
-
 // e2m1 codes of two fp32 values, round to nearest even, saturating at 6: the
 // hardware conversion (the same rounding as e2m1_encode, sign of zero kept);
 // `lo` goes to the low nibble.
@@ -87,10 +64,27 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return b;
 }
 
+// The e2m1 code of a bf16 value v divided by a nonzero e4m3 scale d, equal to
+// e2m1 of the correctly rounded fp32 quotient fl(v / d) without dividing.
+// Why it is exact: v has at most 8 significant bits and d at most 4, so
+// v / d is either exactly one of the e2m1 rounding thresholds t (0.25, 0.75,
+// ..., 5; then v = t d, a number of at most 7 bits) or at least ~2^-12 of t
+// away from every one of them, far beyond fp32 rounding. With r ~ 1/d,
+// q0 = v r and the residual e = v - q0 d (exact, one fused multiply-add), the
+// corrected q1 = q0 + e r (Markstein's FMA-based refinement of a quotient) is
+// within a fraction of an ulp of v / d: on the same side of every threshold,
+// and exactly t at a tie, where the conversion applies ties-to-even. The sign
+// is v's, so that -0 keeps its code (the sum in the refinement would give +0).
+__device__ __forceinline__ float quotient_for_e2m1(float v, float d, float r) {
+  const float q0 = v * r;
+  return copysignf(fmaf(fmaf(-q0, d, v), r, q0), v);
+}
+
 // NVFP4 codec for eight values per lane, a lane pair (2j, 2j+1) holding one
-// 16-value block: the pair's block scale (e4m3 of amax / 6) and this lane's
-// four packed code bytes (value 2i in the low nibble of byte i). Every lane
-// of the warp must take part (one shuffle).
+// 16-value block: the pair's block scale (e4m3 of amax / 6, a correctly
+// rounded division) and this lane's four packed code bytes (value 2i in the
+// low nibble of byte i). `v` holds fp32 values exact in bf16. Every lane of
+// the warp must take part (one shuffle).
 __device__ __forceinline__ void quantize_oct(const float (&v)[8], uint32_t& codes, uint32_t& scale) {
   float amax = 0.0f;
 #pragma unroll
@@ -100,8 +94,10 @@ __device__ __forceinline__ void quantize_oct(const float (&v)[8], uint32_t& code
   const float d = e4m3_decode(scale);
   codes = 0u;
   if (d != 0.0f) {  // an underflowed block keeps all-zero codes
+    const float r = __frcp_rn(d);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) codes |= e2m1x2(__fdiv_rn(v[2 * i], d), __fdiv_rn(v[2 * i + 1], d)) << (8 * i);
+    for (int i = 0; i < 4; ++i)
+      codes |= e2m1x2(quotient_for_e2m1(v[2 * i], d, r), quotient_for_e2m1(v[2 * i + 1], d, r)) << (8 * i);
   }
 }
 

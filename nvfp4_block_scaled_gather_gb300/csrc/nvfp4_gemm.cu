@@ -256,7 +256,7 @@ __device__ __forceinline__ void quantize_feature(float v, int lane, uint32_t& wo
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
   const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
   const float dsc = e4m3_decode(sc);
-  const uint32_t code = dsc != 0.0f ? e2m1_encode(__fdiv_rn(v, dsc)) : 0u;
+  const uint32_t code = dsc != 0.0f ? e2m1_encode(quotient_for_e2m1(v, dsc, __frcp_rn(dsc))) : 0u;
   uint32_t w = code << (4 * (lane & 7));
   w |= __shfl_xor_sync(~0u, w, 1);
   w |= __shfl_xor_sync(~0u, w, 2);

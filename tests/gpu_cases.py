@@ -229,6 +229,36 @@ def edge_rows(R, K, seed=0):
     return np.asarray(O.f64_to_bf16_bits(x.astype(np.float64)))
 
 
+def quotient_sweep_blocks() -> np.ndarray:
+    """bf16 bits, 16-value blocks covering every nonzero e4m3 scale code c and,
+    for each, every bf16 magnitude from d/8 to 6d (d the value of c) in both
+    signs: element 0 of a block is +-6d, the block maximum, so the block scale
+    is exactly c, and the other 15 carry the sweep, so v / d passes every
+    e2m1 rounding threshold and its neighbours; the padding of the last
+    block of each code alternates +0 and -0. Returns [n_blocks, 16]."""
+    pos = np.arange(0x0001, 0x7F80, dtype=np.uint16)             # positive finite bf16
+    mags = O.bf16_bits_to_f64(pos)
+    out = []
+    for c in range(1, 0x7F):
+        d = float(O.e4m3_decode(np.array([c], np.uint8))[0])
+        sel = pos[(mags >= d / 8) & (mags <= 6 * d)]
+        sweep = np.concatenate([sel, sel | np.uint16(0x8000)])
+        pad = (-sweep.size) % 15
+        sweep = np.concatenate([sweep, np.where(np.arange(pad) % 2 == 0, 0x0000, 0x8000).astype(np.uint16)])
+        body = sweep.reshape(-1, 15)
+        top = O.f64_to_bf16_bits(np.array([6 * d]))[0]
+        head = np.where(np.arange(body.shape[0]) % 2 == 0, top, top | 0x8000).astype(np.uint16)
+        out.append(np.concatenate([head[:, None], body], axis=1))
+    return np.concatenate(out)
+
+
+def blocks_as_rows(blocks: np.ndarray, R: int, K: int) -> np.ndarray:
+    """Lay 16-value blocks out row-major over [R, K] bf16 bits, zero-padded."""
+    flat = blocks.reshape(-1)
+    assert flat.size <= R * K
+    return np.concatenate([flat, np.zeros(R * K - flat.size, np.uint16)]).reshape(R, K)
+
+
 def check_groups(host, ref_row_slot, ref_offs, ref_gexp, S):
     G = len(ref_gexp)
     assert host["G"] == G and host["R"] == len(ref_row_slot)

@@ -20,8 +20,9 @@ import torch
 from nvfp4_block_scaled_gather_gb300 import _native as N
 from nvfp4_block_scaled_gather_gb300.synthetic import make_edge_weights
 from oracle import nvfp4_moe as O
-from tests.gpu_cases import (GEMM_TOL, LAYER_TOL, assert_swiglu_close, bf16_to_np, check_stages_against_oracle,
-                             chunk32_bytes, edge_rows, np_to_bf16, rel_fro, row_scales, run_stages, weights_from)
+from tests.gpu_cases import (GEMM_TOL, LAYER_TOL, assert_swiglu_close, bf16_to_np, blocks_as_rows,
+                             check_stages_against_oracle, chunk32_bytes, edge_rows, np_to_bf16, quotient_sweep_blocks,
+                             rel_fro, row_scales, run_stages, weights_from)
 
 pytestmark = pytest.mark.gpu
 
@@ -157,4 +158,94 @@ def test_layer_edge_scales(cuda):
     with np.errstate(over="ignore"):
         ref = O.moe_layer(x_np, ids.numpy(), tw.numpy(), w_np, E)
     assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(y)), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
+    assert N.check_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# The device codec divides by the block scale without a division: from the
+# reciprocal of d it refines the quotient with one fused multiply-add
+# (Markstein's method) and converts that. The oracle divides (correctly
+# rounded fp32 quotient). These sweeps hold every nonzero scale code against
+# every bf16 magnitude from d/8 to 6d, both signs and +-0, in each kernel
+# that quantizes: the row quantizer, the one-launch decode front end and the
+# SwiGLU requantizer. (The GEMM's fused epilogue calls the same device
+# function and is held bit-equal to the SwiGLU requantizer above.)
+# ---------------------------------------------------------------------------
+
+def _sweep_case(K):
+    blocks = quotient_sweep_blocks()
+    R = -(-blocks.size // K)
+    return blocks, blocks_as_rows(blocks, R, K), R
+
+
+def _assert_every_scale_code(scales, n_blocks):
+    assert set(np.asarray(scales).reshape(-1)[:n_blocks].tolist()) == set(range(1, 0x7F))
+
+
+def test_quantizer_every_scale_code_and_quotient(cuda):
+    K = 4096
+    blocks, rows, R = _sweep_case(K)
+    mg = (R // 3, R // 3 + 5, R - 2 * (R // 3) - 5)
+    offs = np.concatenate([[0], np.cumsum(mg)])
+    ref_p, ref_sf = O.quantize_rows(rows, offs)
+    scales = row_scales(ref_sf, offs, K)
+    _assert_every_scale_code(scales, blocks.shape[0])
+    G = _groups_for(mg, cuda)
+    for layout in (N.SF_ATOM128, N.SF_CHUNK32):
+        packed = torch.zeros(R, K // 2, dtype=torch.uint8, device=cuda)
+        sf = torch.zeros(N.sf_bytes(R, len(mg), K, layout), dtype=torch.uint8, device=cuda)
+        N.nvfp4_quantize_rows(np_to_bf16(rows, cuda), G, packed, sf, layout)
+        assert np.array_equal(packed.cpu().numpy(), ref_p), layout
+        want = ref_sf if layout == N.SF_ATOM128 else chunk32_bytes(scales, offs, K)
+        assert np.array_equal(sf[:want.size].cpu().numpy(), want), layout
+    assert N.check_status() == 0
+
+
+def test_decode_front_end_every_scale_code_and_quotient(cuda):
+    """The one-launch route + gather + quantize (T*k <= 32) on the sweep: 8
+    tokens, k = 1, token t routed to expert t, so routed row t is x[t]."""
+    T, E = 8, 8
+    blocks = quotient_sweep_blocks()
+    H = -(-blocks.size // (T * 64)) * 64
+    x_np = blocks_as_rows(blocks, T, H)
+    offs = np.arange(T + 1)
+    ref_p, ref_sf = O.quantize_rows(x_np, offs)
+    scales = row_scales(ref_sf, offs, H)
+    _assert_every_scale_code(scales, blocks.shape[0])
+    ids = torch.arange(T, dtype=torch.int32, device=cuda).reshape(T, 1)
+    G = N.Groups(T, 1, E, cuda)
+    xq = torch.zeros(T, H // 2, dtype=torch.uint8, device=cuda)
+    xsf = torch.zeros(N.sf_bytes(T, E, H, N.SF_CHUNK32), dtype=torch.uint8, device=cuda)
+    N.moe_route_gather_quantize(ids, np_to_bf16(x_np, cuda), E, G, xq, xsf)
+    assert np.array_equal(xq.cpu().numpy(), ref_p)
+    want = chunk32_bytes(scales, offs, H)
+    assert np.array_equal(xsf[:want.size].cpu().numpy(), want)
+    assert N.check_status() == 0
+
+
+def test_swiglu_requantizer_every_scale_code_and_quotient(cuda):
+    """swiglu_quantize_grouped with gate = 32 and up = v / 32 (globals 1): in
+    fp32 and in the oracle silu(32) * (v / 32) rounds to v, so h is the sweep
+    itself and its codes must equal the oracle's quantization of the sweep."""
+    I = 4096
+    blocks, rows, R = _sweep_case(I)
+    mg = (R // 2, R - R // 2)
+    E = len(mg)
+    offs = np.concatenate([[0], np.cumsum(mg)])
+    v = O.bf16_bits_to_f64(rows).astype(np.float32)
+    d13 = np.concatenate([np.full((R, I), 32.0, np.float32), v / np.float32(32.0)], axis=1)
+    ones = np.ones((E, 2), np.float32)
+    assert np.array_equal(O.swiglu(d13, offs, np.arange(E), ones), rows)
+    ref_p, ref_sf = O.quantize_rows(rows, offs)
+    scales = row_scales(ref_sf, offs, I)
+    _assert_every_scale_code(scales, blocks.shape[0])
+    G = _groups_for(mg, cuda)
+    d13_d, g_d = torch.from_numpy(d13).to(cuda), torch.from_numpy(ones).to(cuda)
+    for layout in (N.SF_ATOM128, N.SF_CHUNK32):
+        hq = torch.zeros(R, I // 2, dtype=torch.uint8, device=cuda)
+        hsf = torch.zeros(N.sf_bytes(R, E, I, layout), dtype=torch.uint8, device=cuda)
+        N.swiglu_quantize_grouped(d13_d, G, g_d, hq, hsf, layout)
+        assert np.array_equal(hq.cpu().numpy(), ref_p), layout
+        want = ref_sf if layout == N.SF_ATOM128 else chunk32_bytes(scales, offs, I)
+        assert np.array_equal(hsf[:want.size].cpu().numpy(), want), layout
     assert N.check_status() == 0
