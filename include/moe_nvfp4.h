@@ -35,8 +35,9 @@
  *       ((m/128)*(Kc/4) + c/4)*512 + (m%32)*16 + ((m/32)%4)*4 + (c%4).
  *   - activations carry no global scale (alpha = 1): block scale =
  *     e4m3_rne_satfinite(amax/6); codes = e2m1_rne_satfinite(x/scale); both
- *     divisions correctly rounded fp32; a block whose scale is 0 has all-zero
- *     codes.
+ *     quotients those of correctly rounded fp32 division (the kernels reach
+ *     the same codes by reciprocal and refinement); a block whose scale is 0
+ *     has all-zero codes.
  *   - weights carry one fp32 global per projection (weight_scale_2); gate and
  *     up have their own (second page, "Different globals on the two halves").
  *

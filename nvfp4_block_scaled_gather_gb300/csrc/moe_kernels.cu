@@ -173,13 +173,12 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
   float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
-  const uint32_t s = e4m3_encode(__fdiv_rn(amax, 6.0f));
-  const float d = e4m3_decode(s);
+  const uint32_t s = block_scale_code(amax);
   uint32_t codes = 0u;
-  if (d != 0.0f) {  // an underflowed block keeps all-zero codes
-    const float r = __frcp_rn(d);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) codes |= e2m1_encode(quotient_for_e2m1(v[i], d, r)) << (4 * i);
+  if (s != 0u) {  // an underflowed block keeps all-zero codes
+    const float d = e4m3_value(s), r = rcp_approx(d);
+    codes = e2m1x2(block_quotient(v[0], d, r), block_quotient(v[1], d, r)) |
+            (e2m1x2(block_quotient(v[2], d, r), block_quotient(v[3], d, r)) << 8);
   }
   const uint32_t s1 = __shfl_down_sync(~0u, s, 4), s2 = __shfl_down_sync(~0u, s, 8),
                  s3 = __shfl_down_sync(~0u, s, 12);

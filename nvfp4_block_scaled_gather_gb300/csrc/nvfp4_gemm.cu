@@ -254,9 +254,12 @@ __device__ __forceinline__ void quantize_feature(float v, int lane, uint32_t& wo
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 4));
   amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 8));
-  const uint32_t sc = e4m3_encode(__fdiv_rn(amax, 6.0f));
-  const float dsc = e4m3_decode(sc);
-  const uint32_t code = dsc != 0.0f ? e2m1_encode(quotient_for_e2m1(v, dsc, __frcp_rn(dsc))) : 0u;
+  const uint32_t sc = block_scale_code(amax);
+  uint32_t code = 0u;  // an underflowed block keeps all-zero codes
+  if (sc != 0u) {
+    const float dsc = e4m3_value(sc);
+    code = e2m1x2(block_quotient(v, dsc, rcp_approx(dsc)), 0.0f) & 0xFu;
+  }
   uint32_t w = code << (4 * (lane & 7));
   w |= __shfl_xor_sync(~0u, w, 1);
   w |= __shfl_xor_sync(~0u, w, 2);

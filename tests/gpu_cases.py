@@ -252,6 +252,21 @@ def quotient_sweep_blocks() -> np.ndarray:
     return np.concatenate(out)
 
 
+def amax_sweep_blocks() -> np.ndarray:
+    """bf16 bits, one 16-value block per positive finite bf16 value a (0x0001
+    .. 0x7F7F): element 0 is +-a, the block maximum, so the block scale
+    runs over e4m3(a / 6) for every a, through the subnormal scales, the
+    zero-scale (underflow) blocks and the saturated ones; the other 15 are
+    bf16(a j / 16), j = 1 .. 15, with alternating signs. Returns [32639, 16]."""
+    a = np.arange(0x0001, 0x7F80, dtype=np.uint16)
+    av = O.bf16_bits_to_f64(a)
+    j = np.arange(1, 16, dtype=np.float64)
+    body = O.f64_to_bf16_bits(av[:, None] * j[None, :] / 16.0)
+    body = np.where(np.arange(15) % 2 == 1, body | np.uint16(0x8000), body).astype(np.uint16)
+    head = np.where(np.arange(a.size) % 2 == 0, a, a | np.uint16(0x8000)).astype(np.uint16)
+    return np.concatenate([head[:, None], body], axis=1)
+
+
 def blocks_as_rows(blocks: np.ndarray, R: int, K: int) -> np.ndarray:
     """Lay 16-value blocks out row-major over [R, K] bf16 bits, zero-padded."""
     flat = blocks.reshape(-1)

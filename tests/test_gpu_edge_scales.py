@@ -20,7 +20,7 @@ import torch
 from nvfp4_block_scaled_gather_gb300 import _native as N
 from nvfp4_block_scaled_gather_gb300.synthetic import make_edge_weights
 from oracle import nvfp4_moe as O
-from tests.gpu_cases import (GEMM_TOL, LAYER_TOL, assert_swiglu_close, bf16_to_np, blocks_as_rows,
+from tests.gpu_cases import (GEMM_TOL, LAYER_TOL, amax_sweep_blocks, assert_swiglu_close, bf16_to_np, blocks_as_rows,
                              check_stages_against_oracle, chunk32_bytes, edge_rows, np_to_bf16, quotient_sweep_blocks,
                              rel_fro, row_scales, run_stages, weights_from)
 
@@ -162,34 +162,43 @@ def test_layer_edge_scales(cuda):
 
 
 # ---------------------------------------------------------------------------
-# The device codec divides by the block scale without a division: from the
-# reciprocal of d it refines the quotient with one fused multiply-add
-# (Markstein's method) and converts that. The oracle divides (correctly
-# rounded fp32 quotient). These sweeps hold every nonzero scale code against
-# every bf16 magnitude from d/8 to 6d, both signs and +-0, in each kernel
-# that quantizes: the row quantizer, the one-launch decode front end and the
-# SwiGLU requantizer. (The GEMM's fused epilogue calls the same device
-# function and is held bit-equal to the SwiGLU requantizer above.)
+# The device codec does not divide: it converts with the hardware's e4m3 and
+# e2m1 conversions, and forms each quotient from an approximate reciprocal
+# and one fused multiply-add refinement (Markstein's method). The oracle
+# divides (correctly rounded fp32 quotients) and rounds in software. Two
+# sweeps hold the two against each other in each kernel that quantizes (the
+# row quantizer, the one-launch decode front end, the SwiGLU requantizer):
+#   "quotient": every nonzero scale code with every bf16 magnitude from d/8
+#       to 6d, both signs and +-0 (every e2m1 threshold of every scale);
+#   "amax": every positive finite bf16 block maximum (every e4m3 rounding
+#       of amax / 6: subnormal, zero and saturated scales included).
+# (The GEMM's fused epilogue calls the same device functions and is held
+# bit-equal to the SwiGLU requantizer elsewhere.)
 # ---------------------------------------------------------------------------
 
-def _sweep_case(K):
-    blocks = quotient_sweep_blocks()
+SWEEPS = {"quotient": quotient_sweep_blocks, "amax": amax_sweep_blocks}
+
+
+def _sweep_case(sweep, K):
+    blocks = SWEEPS[sweep]()
     R = -(-blocks.size // K)
     return blocks, blocks_as_rows(blocks, R, K), R
 
 
-def _assert_every_scale_code(scales, n_blocks):
-    assert set(np.asarray(scales).reshape(-1)[:n_blocks].tolist()) == set(range(1, 0x7F))
+def _assert_scale_codes(scales, n_blocks, sweep):
+    codes = set(np.asarray(scales).reshape(-1)[:n_blocks].tolist())
+    assert codes == (set(range(1, 0x7F)) if sweep == "quotient" else set(range(0x7F))), sweep
 
 
-def test_quantizer_every_scale_code_and_quotient(cuda):
+@pytest.mark.parametrize("sweep", sorted(SWEEPS))
+def test_quantizer_codec_sweep(cuda, sweep):
     K = 4096
-    blocks, rows, R = _sweep_case(K)
+    blocks, rows, R = _sweep_case(sweep, K)
     mg = (R // 3, R // 3 + 5, R - 2 * (R // 3) - 5)
     offs = np.concatenate([[0], np.cumsum(mg)])
     ref_p, ref_sf = O.quantize_rows(rows, offs)
     scales = row_scales(ref_sf, offs, K)
-    _assert_every_scale_code(scales, blocks.shape[0])
+    _assert_scale_codes(scales, blocks.shape[0], sweep)
     G = _groups_for(mg, cuda)
     for layout in (N.SF_ATOM128, N.SF_CHUNK32):
         packed = torch.zeros(R, K // 2, dtype=torch.uint8, device=cuda)
@@ -201,17 +210,18 @@ def test_quantizer_every_scale_code_and_quotient(cuda):
     assert N.check_status() == 0
 
 
-def test_decode_front_end_every_scale_code_and_quotient(cuda):
+@pytest.mark.parametrize("sweep", sorted(SWEEPS))
+def test_decode_front_end_codec_sweep(cuda, sweep):
     """The one-launch route + gather + quantize (T*k <= 32) on the sweep: 8
     tokens, k = 1, token t routed to expert t, so routed row t is x[t]."""
     T, E = 8, 8
-    blocks = quotient_sweep_blocks()
+    blocks = SWEEPS[sweep]()
     H = -(-blocks.size // (T * 64)) * 64
     x_np = blocks_as_rows(blocks, T, H)
     offs = np.arange(T + 1)
     ref_p, ref_sf = O.quantize_rows(x_np, offs)
     scales = row_scales(ref_sf, offs, H)
-    _assert_every_scale_code(scales, blocks.shape[0])
+    _assert_scale_codes(scales, blocks.shape[0], sweep)
     ids = torch.arange(T, dtype=torch.int32, device=cuda).reshape(T, 1)
     G = N.Groups(T, 1, E, cuda)
     xq = torch.zeros(T, H // 2, dtype=torch.uint8, device=cuda)
@@ -223,12 +233,13 @@ def test_decode_front_end_every_scale_code_and_quotient(cuda):
     assert N.check_status() == 0
 
 
-def test_swiglu_requantizer_every_scale_code_and_quotient(cuda):
+@pytest.mark.parametrize("sweep", sorted(SWEEPS))
+def test_swiglu_requantizer_codec_sweep(cuda, sweep):
     """swiglu_quantize_grouped with gate = 32 and up = v / 32 (globals 1): in
     fp32 and in the oracle silu(32) * (v / 32) rounds to v, so h is the sweep
     itself and its codes must equal the oracle's quantization of the sweep."""
     I = 4096
-    blocks, rows, R = _sweep_case(I)
+    blocks, rows, R = _sweep_case(sweep, I)
     mg = (R // 2, R - R // 2)
     E = len(mg)
     offs = np.concatenate([[0], np.cumsum(mg)])
@@ -238,7 +249,7 @@ def test_swiglu_requantizer_every_scale_code_and_quotient(cuda):
     assert np.array_equal(O.swiglu(d13, offs, np.arange(E), ones), rows)
     ref_p, ref_sf = O.quantize_rows(rows, offs)
     scales = row_scales(ref_sf, offs, I)
-    _assert_every_scale_code(scales, blocks.shape[0])
+    _assert_scale_codes(scales, blocks.shape[0], sweep)
     G = _groups_for(mg, cuda)
     d13_d, g_d = torch.from_numpy(d13).to(cuda), torch.from_numpy(ones).to(cuda)
     for layout in (N.SF_ATOM128, N.SF_CHUNK32):
