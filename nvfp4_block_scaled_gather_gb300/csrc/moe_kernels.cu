@@ -187,22 +187,6 @@ __device__ __forceinline__ void quantize_quad_store(const float (&v)[4], bool ac
   if ((lane & 15) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
-// Lane pairs (2j, 2j+1) of a warp hold one 16-value block, eight values each;
-// eight lanes hold the four blocks of one 4-byte scale word. Each lane writes
-// its four packed bytes; the first lane of each eight writes the word. Lanes
-// that are not `active` compute along (shuffles need the full warp) but write
-// nothing; an 8-lane group is either wholly active or wholly not.
-__device__ __forceinline__ void quantize_oct_store(const float (&v)[8], bool active, int lane,
-                                                   uint8_t* __restrict__ packed_dst, uint32_t* __restrict__ word) {
-  uint32_t codes, s;
-  quantize_oct(v, codes, s);
-  const uint32_t s1 = __shfl_down_sync(~0u, s, 2), s2 = __shfl_down_sync(~0u, s, 4),
-                 s3 = __shfl_down_sync(~0u, s, 6);
-  if (!active) return;
-  *reinterpret_cast<uint32_t*>(packed_dst) = codes;
-  if ((lane & 7) == 0) *word = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-}
-
 // Token-scale layouts (include/moe_nvfp4.h): per group 128-row atoms, or per
 // 32-row GEMM chunk one 512-byte atom per 64 K values whose 16-byte row i
 // holds chunk row i's four scales in its first word (other words zero).
@@ -211,11 +195,13 @@ constexpr int kRowsAtom = 128;
 struct ScaleTarget {
   uint8_t* base;  // the CTA's row block region
   int layout, Kc;
-  // word holding scale columns c..c+3 (c % 4 == 0) of row m of the block
-  __device__ __forceinline__ uint32_t* word(int m, int c) const {
-    const uint32_t off = layout == MOE_SF_ATOM128 ? sf_atom_offset(m, c, Kc) : (uint32_t)(c >> 2) * 512u + m * 16u;
-    return reinterpret_cast<uint32_t*>(base + off);
+  // scale byte of column c of row m of the block
+  __device__ __forceinline__ uint8_t* byte(int m, int c) const {
+    return base + (layout == MOE_SF_ATOM128 ? sf_atom_offset(m, c, Kc)
+                                            : (uint32_t)(c >> 2) * 512u + m * 16u + (uint32_t)(c & 3));
   }
+  // word holding scale columns c..c+3 (c % 4 == 0) of row m of the block
+  __device__ __forceinline__ uint32_t* word(int m, int c) const { return reinterpret_cast<uint32_t*>(byte(m, c)); }
   // zero every word of atoms [a0, a0 + na) that no real row (< nvalid) fills
   __device__ __forceinline__ void zero_rest(int a0, int na, int nvalid) const {
     uint32_t* words = reinterpret_cast<uint32_t*>(base + (size_t)a0 * 512);
@@ -249,13 +235,15 @@ __device__ __forceinline__ int routed_blocks(const moe_groups_t& g, int layout) 
 }
 
 constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K) for the SwiGLU and small-batch kernels
-constexpr int kQuantCols = 256;    // K values per CTA of the quantizer
+constexpr int kQuantCols = 512;    // K values per CTA of the quantizer: one row per warp pass
 
 // ---------------------------------------------------------------------------
-// a3 / a6 quantize (with optional a2 gather). Grid: (row block, 256-value
-// column chunk); CTAs past the routed block count exit. Each lane quantizes 8
-// values from one 16-byte load, a lane pair one 16-value block; scale words no
-// real row fills are zeroed.
+// a3 / a6 quantize (with optional a2 gather). Grid: (row block, 512-value
+// column chunk); CTAs past the routed block count exit. Lane l of a warp
+// quantizes 16-value block l of a row from two 16-byte loads and writes its
+// 8 code bytes and its scale byte (four lanes fill a scale word); the eight
+// warps take rows w, w + 8, ..., two rows in flight. Scale words no real row
+// fills are zeroed.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ src, int src_k, int K,
                                                             moe_groups_t g, int layout, uint8_t* __restrict__ packed,
@@ -270,10 +258,9 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
   const RowBlock rb{c.x, c.y, c.z};
   const int Kc = K / 16;
   const int kc0 = blockIdx.y * kQuantCols;
-  const int kcount = min(kQuantCols, K - kc0);
-  const int octs = kcount / 8;
-  const int total = rb.nvalid * octs;
-  const int lane = threadIdx.x & 31;
+  const int kcount = min(kQuantCols, K - kc0);  // a multiple of 64
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool lane_on = 16 * lane < kcount;       // every lane but in a short last chunk
   const ScaleTarget st{sf + (size_t)blk * 128 * Kc, layout, Kc};  // either layout: 128*Kc bytes per block
   // source row of each of the block's rows, read once
   __shared__ int s_src[kRowsAtom];
@@ -282,32 +269,38 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
     s_src[threadIdx.x] = src_k > 0 ? ld_cg(g.row_slot + r) / src_k : r;
   }
   __syncthreads();
-  // Up to kBatch of this warp's items loaded before any is quantized, so that
-  // a block of many rows costs one memory round trip per kBatch, not per row.
-  constexpr int kBatch = 2;  // 2 in flight: 40 registers, six CTAs of 256 threads per SM
-  for (int base0 = (threadIdx.x & ~31); base0 < total; base0 += kBatch * blockDim.x) {
-    uint4 u[kBatch];
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kBatch = 2;  // rows in flight per warp
+  for (int m0 = warp; m0 < rb.nvalid; m0 += kBatch * kWarps) {
+    uint4 u[kBatch][2];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int item = base0 + j * blockDim.x + lane;
-      u[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (item < total) {
-        const int m = item / octs, o = item - m * octs;
-        u[j] = ld_cg(reinterpret_cast<const uint4*>(src + (size_t)s_src[m] * K + kc0 + 8 * o));
+      const int m = m0 + j * kWarps;
+      u[j][0] = u[j][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (m < rb.nvalid && lane_on) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + (size_t)s_src[m] * K + kc0 + 16 * lane);
+        u[j][0] = ld_cg(p);
+        u[j][1] = ld_cg(p + 1);
       }
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int base = base0 + j * blockDim.x;  // the same for the whole warp
-      if (base >= total) break;
-      const int item = base + lane;
-      const bool active = item < total;
-      const int m = active ? item / octs : 0;
-      const int o = active ? item - m * octs : 0;
-      float v[8];
-      bf16x8_to_f32(u[j], v);
-      quantize_oct_store(v, active, lane, packed + (size_t)(rb.row0 + m) * (K / 2) + (kc0 + 8 * o) / 2,
-                         st.word(m, (kc0 + 8 * o) / 16));
+      const int m = m0 + j * kWarps;  // the same for the whole warp
+      if (m >= rb.nvalid) break;
+      const uint32_t w[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w, u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      uint2 codes;
+      uint32_t scale;
+      quantize_block16(v, codes, scale);
+      if (lane_on) {
+        *reinterpret_cast<uint2*>(packed + (size_t)(rb.row0 + m) * (K / 2) + kc0 / 2 + 8 * lane) = codes;
+        *st.byte(m, kc0 / 16 + lane) = (uint8_t)scale;
+      }
     }
   }
   st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);

@@ -37,11 +37,12 @@ __device__ __forceinline__ float rcp_approx(float d) {
 // error, so converting the result to e2m1 or e4m3 gives the code of the
 // correctly rounded quotient. Checked for every nonzero e4m3 d, every bf16 v
 // with |v| <= 9 d (the codec's range) in both signs and every r within three
-// ulps of 1 / d; for d = 6 (the block scale), every finite bf16 v. The sign is
-// v's, so that -0 keeps its code (the refinement's sum would give +0).
+// ulps of 1 / d; for d = 6 (the block scale), every finite bf16 v. The
+// residual is formed as q0 d - v and subtracted, so that v = -0 gives -0 (a
+// negative value that rounds to zero keeps its sign).
 __device__ __forceinline__ float block_quotient(float v, float d, float r) {
   const float q0 = v * r;
-  return copysignf(fmaf(fmaf(-q0, d, v), r, q0), v);
+  return fmaf(-fmaf(q0, d, -v), r, q0);
 }
 
 // e2m1 codes of two fp32 values (`lo` in the low nibble): nearest-even on
@@ -72,31 +73,23 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return f;
 }
 
-// NVFP4 codec for eight values per lane, a lane pair (2j, 2j+1) holding one
-// 16-value block: the pair's block scale code and this lane's four packed
-// code bytes (value 2i in the low nibble of byte i). `v` holds fp32 values
-// exact in bf16. Every lane of the warp must take part (one shuffle).
-__device__ __forceinline__ void quantize_oct(const float (&v)[8], uint32_t& codes, uint32_t& scale) {
+// NVFP4 codec for one 16-value block held by one lane: its block scale code
+// and its eight packed code bytes (value 2i in the low nibble of byte i; bytes
+// 0-3 in codes.x). `v` holds fp32 values exact in bf16.
+__device__ __forceinline__ void quantize_block16(const float (&v)[16], uint2& codes, uint32_t& scale) {
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
   scale = block_scale_code(amax);
-  codes = 0u;
+  codes = make_uint2(0u, 0u);
   if (scale != 0u) {  // an underflowed block keeps all-zero codes
     const float d = e4m3_value(scale), r = rcp_approx(d);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      codes |= e2m1x2(block_quotient(v[2 * i], d, r), block_quotient(v[2 * i + 1], d, r)) << (8 * i);
+    for (int i = 0; i < 4; ++i) {
+      codes.x |= e2m1x2(block_quotient(v[2 * i], d, r), block_quotient(v[2 * i + 1], d, r)) << (8 * i);
+      codes.y |= e2m1x2(block_quotient(v[8 + 2 * i], d, r), block_quotient(v[9 + 2 * i], d, r)) << (8 * i);
+    }
   }
-}
-
-// Eight bf16 values (one 16-byte load) as fp32.
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
-  v[0] = bf16_to_f32(u.x & 0xFFFFu); v[1] = bf16_to_f32(u.x >> 16);
-  v[2] = bf16_to_f32(u.y & 0xFFFFu); v[3] = bf16_to_f32(u.y >> 16);
-  v[4] = bf16_to_f32(u.z & 0xFFFFu); v[5] = bf16_to_f32(u.z >> 16);
-  v[6] = bf16_to_f32(u.w & 0xFFFFu); v[7] = bf16_to_f32(u.w >> 16);
 }
 
 // Byte offset of scale (row m, column c) in a region of 128-row atoms with

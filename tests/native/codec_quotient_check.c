@@ -1,13 +1,13 @@
 /* Exhaustive check of the device codec's quotient method (plain C, fp32).
  *
  * The device forms v / d from an approximate reciprocal r and one fused
- * multiply-add refinement (Markstein's method): q0 = v r, q1 = q0 +
- * (v - q0 d) r, sign of v. This program checks, for every nonzero e4m3 scale
- * d and every bf16 v with |v| <= 9 d in both signs (+-0 included), and for
- * every r within three ulps of the correctly rounded 1 / d, that q1 converts
- * to the same e2m1 code as the correctly rounded quotient v / d; and, for
- * d = 6 (the block scale amax / 6) and every finite bf16 amax, the same e4m3
- * code. The conversions here are written from the value sets (nearest, ties
+ * multiply-add refinement (Markstein's method): q0 = v r, q1 = q0 -
+ * (q0 d - v) r, the residual formed so that v = -0 gives -0. This program
+ * checks, for every nonzero e4m3 scale d and every bf16 v with |v| <= 9 d in
+ * both signs (+-0 included), and for every r within three ulps of the
+ * correctly rounded 1 / d, that q1 converts to the same e2m1 code as the
+ * correctly rounded quotient v / d; and, for d = 6 (the block scale amax / 6)
+ * and every finite bf16 amax, the same e4m3 code. The conversions here are written from the value sets (nearest, ties
  * to the even code, saturating), independently of the oracle and the device.
  * Exit status 0 and the counts on stdout when every case agrees. */
 #include <math.h>
@@ -54,7 +54,7 @@ static float refined(float v, float d, float r) {
 #ifdef WITHOUT_REFINEMENT /* the check must reject the plain product v r */
   return q0;
 #else
-  return copysignf(fmaf(fmaf(-q0, d, v), r, q0), v);
+  return fmaf(-fmaf(q0, d, -v), r, q0);
 #endif
 }
 
