@@ -114,8 +114,8 @@ struct GemmJob {
 // front != nullptr (small batches, S = T*k <= 32; early must be false):
 // every CTA routes the slots itself from topk_ids (which must be two or more
 // launches old) and, before waiting for the previous kernel (the
-// gather-quantize of these rows), prefetches into L2 the first weight stages
-// of the units the first claims hand out.
+// gather-quantize of these rows), claims its first unit and issues that
+// unit's first weight stages.
 struct SmallFront {
   const int32_t* topk_ids;
   int S;

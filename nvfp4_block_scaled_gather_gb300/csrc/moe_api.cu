@@ -390,7 +390,7 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   // route, then gather+quantize; either clears the GEMM launch's work counters. The GEMM
   // launch starts on weights before the previous kernel ends: with a group table two launches
   // old it claims units and streams them (early); for decode-sized batches it routes the
-  // slots itself from topk_ids and warms L2 with its first weight stages while it waits.
+  // slots itself from topk_ids and issues its first unit's first weight stages while it waits.
   // Token blocks (and scale layout): 128 rows for prefill-sized batches, else 32.
   const bool small = S <= kSmallRouteSlots;
   const int layout = layer_sf_layout(S, E);

@@ -100,9 +100,8 @@ struct GemmArgs {
   int* exit_ctr;            // njobs == 2: CTAs done; the last one zeroes the counters again
   // small != 0: T*k <= 32 slots; every CTA routes them itself (one warp)
   // from topk_ids, written two or more launches back, and before waiting for
-  // the previous kernel (the gather-quantize of these rows) prefetches into
-  // L2 the first weight stages of unit blockIdx.x, the unit the first claims
-  // hand out; claims and everything else follow the wait (early must be 0)
+  // the previous kernel (the gather-quantize of these rows) claims its first
+  // unit and issues that unit's first weight stages (early must be 0)
   int small;
   const int32_t* topk_ids;  // [S] slots
   int S, E;
