@@ -31,7 +31,9 @@ if ROOT not in sys.path:
 METRIC = "MoE layer ms/step and weight-stream GB/s (% of HBM roofline) at M=1/8/32"
 FALLBACK_HBM_GBS = 6800.0
 N_ROUTINGS = 20
-GEMM_SRC = os.path.join(ROOT, "nvfp4_block_scaled_gather_gb300", "csrc", "nvfp4_gemm.cu")
+# the GEMM kernel's source: its translation unit and the headers it includes
+GEMM_SRC = [os.path.join(ROOT, "nvfp4_block_scaled_gather_gb300", "csrc", f)
+            for f in ("nvfp4_gemm.cu", "nvfp4_codec.cuh", "ldcg.cuh", "pdl.cuh", "internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "expert_gemms_decode_m1_traffic.txt")
 
 
@@ -84,12 +86,20 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def gemm_source_sha() -> str:
+    """First 16 hex digits of the SHA-256 of the GEMM kernel's source files, in order."""
+    h = hashlib.sha256()
+    for path in GEMM_SRC:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic():
     """ncu DRAM bytes per GEMM launch (decode M=1), if recorded for the
     current kernel source; None when absent or when the kernel changed since."""
     try:
-        with open(GEMM_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        sha = gemm_source_sha()
         kv = {}
         with open(TRAFFIC_FILE) as f:
             for line in f:

@@ -88,3 +88,16 @@ def test_step_bytes_match_the_pages():
     assert bench.expert_bytes(cfg.H, cfg.I) == 14_155_776
     T, G = 1, 8
     assert bench.step_bytes(cfg, G, T) == G * 14_155_776 + 4 * T * cfg.H + 8 * T * cfg.k + 12 * cfg.E
+
+
+def test_recorded_traffic_is_tied_to_the_kernel_source(tmp_path, monkeypatch):
+    """The ncu traffic figure is reported only for the GEMM source it was
+    measured on (its translation unit and headers); any change voids it."""
+    f = tmp_path / "traffic.txt"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    f.write_text(f"kernel_source_sha256_16: {bench.gemm_source_sha()}\ndram_bytes_per_launch: 123456\n")
+    assert bench.recorded_traffic() == 123456
+    f.write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 123456\n")
+    assert bench.recorded_traffic() is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.txt"))
+    assert bench.recorded_traffic() is None
