@@ -475,7 +475,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const float* __restric
 // ---------------------------------------------------------------------------
 // a8 scatter-add: block (token t, 1024-column chunk). Warp 0 orders the
 // token's used slots by grouped row (ascending expert), then every thread
-// accumulates 4 columns in that order in fp32.
+// accumulates 4 columns in that order in fp32, the loads of up to 8 slots
+// in flight together.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restrict__ d2, int H,
                                                            const int32_t* __restrict__ ids,
@@ -520,13 +521,22 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const float* __restri
   if (col >= H) return;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   const int n = s_n;
-  for (int i = 0; i < n; ++i) {
-    const float c = s_coef[i];
-    const float4 d = ld_cg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i] * H + col));
-    a0 = __fmaf_rn(c, d.x, a0);
-    a1 = __fmaf_rn(c, d.y, a1);
-    a2 = __fmaf_rn(c, d.z, a2);
-    a3 = __fmaf_rn(c, d.w, a3);
+  for (int i0 = 0; i0 < n; i0 += 8) {
+    // up to 8 slots' loads in flight, then the sums in slot order
+    float4 d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      d[j] = i0 + j < n ? ld_cg(reinterpret_cast<const float4*>(d2 + (size_t)s_row[i0 + j] * H + col))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (i0 + j >= n) break;
+      const float c = s_coef[i0 + j];
+      a0 = __fmaf_rn(c, d[j].x, a0);
+      a1 = __fmaf_rn(c, d[j].y, a1);
+      a2 = __fmaf_rn(c, d[j].z, a2);
+      a3 = __fmaf_rn(c, d[j].w, a3);
+    }
   }
   const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a0)) |
                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a1)) << 16);
