@@ -235,6 +235,7 @@ __device__ __forceinline__ int routed_blocks(const moe_groups_t& g, int layout) 
 }
 
 constexpr int kColsPerCta = 1024;  // K values per CTA (grid.y covers K) for the SwiGLU and small-batch kernels
+static_assert(kColsPerCta == 4 * kThreads, "the small-batch kernel gives each thread 4 values of a chunk");
 constexpr int kQuantCols = 512;    // K values per CTA of the quantizer: one row per warp pass
 
 // ---------------------------------------------------------------------------
@@ -311,9 +312,10 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
 // 1024-value column chunk). Warp 0 of every CTA routes the <= 32 slots (one
 // per lane): the same rows, groups and tables as route_kernel (rows ascend by
 // (expert, slot); with at most 32 rows no group has more than one 32-row chunk
-// or 128-row scale block); CTA (0, 0) writes the tables. CTA (r, c) then
-// gathers and quantizes column chunk c of routed row r into the 32-row-chunk
-// token layout exactly as quantize_kernel does; CTAs past the routed rows exit.
+// or 128-row scale block); CTA (0, 0) writes the tables. CTA (s, c) loads
+// column chunk c of slot s's token row while warp 0 routes, then quantizes it
+// into slot s's routed row in the 32-row-chunk token layout, exactly as
+// quantize_kernel does; the CTAs of unused slots exit.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const int32_t* __restrict__ ids, int S, int E,
                                                                         moe_groups_t g, int* __restrict__ zero,
@@ -331,7 +333,15 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
     __syncthreads();
   }
   pdl_trigger();
-  __shared__ int s_src[32], s_chunk[32], s_m[32], s_cnt[32], s_R;
+  // This CTA quantizes slot blockIdx.x's row (token blockIdx.x / k): its
+  // values are loaded here, in flight while warp 0 routes.
+  const int kc0 = blockIdx.y * kColsPerCta;
+  const int kcount = min(kColsPerCta, K - kc0);
+  const int q = threadIdx.x;  // this thread's 4 values (kColsPerCta = 4 * kThreads)
+  const bool q_on = q < kcount / 4 && (int)blockIdx.x < S;
+  uint2 xv = make_uint2(0u, 0u);
+  if (q_on) xv = ld_cg(reinterpret_cast<const uint2*>(x + (size_t)(blockIdx.x / k) * K + kc0 + 4 * q));
+  __shared__ int s_chunk[32], s_m[32], s_cnt[32], s_row[32];
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const bool in = lane < S;
@@ -354,9 +364,9 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
     int mx = ok ? n : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(~0u, mx, o));
+    s_row[lane] = ok ? less + rank : -1;
     if (ok) {
       const int row = less + rank;
-      s_src[row] = lane / k;
       s_chunk[row] = gless;
       s_m[row] = rank;
       if (rank == 0) s_cnt[gless] = n;
@@ -376,7 +386,6 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
       g.slot_row[lane] = -1;
     }
     if (lane == 0) {
-      s_R = R;
       if (lead) {
         g.counts[0] = G;
         g.counts[1] = R;
@@ -390,26 +399,17 @@ __global__ void __launch_bounds__(kThreads) route_quantize_small_kernel(const in
     }
   }
   __syncthreads();
-  const int r = blockIdx.x;
-  if (r >= s_R) return;
+  if ((int)blockIdx.x >= S) return;
+  const int r = s_row[blockIdx.x];  // the slot's routed row
+  if (r < 0) return;                // an unused slot has none
   const int Kc = K / 16;
-  const int kc0 = blockIdx.y * kColsPerCta;
-  const int kcount = min(kColsPerCta, K - kc0);
   const int c = s_chunk[r], m = s_m[r];
   const ScaleTarget st{sf + (size_t)c * 128 * Kc, MOE_SF_CHUNK32, Kc};
   const int lane = threadIdx.x & 31;
-  for (int base = (threadIdx.x & ~31); base < kcount / 4; base += blockDim.x) {
-    const int q = base + lane;
-    const bool active = q < kcount / 4;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
-      const uint2 u = ld_cg(reinterpret_cast<const uint2*>(x + (size_t)s_src[r] * K + kc0 + 4 * q));
-      v[0] = bf16_to_f32(u.x & 0xFFFFu);
-      v[1] = bf16_to_f32(u.x >> 16);
-      v[2] = bf16_to_f32(u.y & 0xFFFFu);
-      v[3] = bf16_to_f32(u.y >> 16);
-    }
-    quantize_quad_store(v, active, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2,
+  if ((threadIdx.x & ~31) < kcount / 4) {  // warps with values (whole warps: kcount % 64 == 0)
+    const float v[4] = {bf16_to_f32(xv.x & 0xFFFFu), bf16_to_f32(xv.x >> 16), bf16_to_f32(xv.y & 0xFFFFu),
+                        bf16_to_f32(xv.y >> 16)};
+    quantize_quad_store(v, q_on, lane, packed + (size_t)r * (K / 2) + (kc0 + 4 * q) / 2,
                         st.word(m, (kc0 + 4 * q) / 16));
   }
   // the chunk's first row also zeroes the words no row fills in these atoms
