@@ -347,11 +347,13 @@ def gpu_bench(args, rank, world):
                 gemm_bytes.append(gemms_launch_bytes(c, it["G"], it["R"]))
         return {n: statistics.mean(v) for n, v in acc.items()}, statistics.mean(gemm_bytes)
 
-    def time_e2e(c, items, steps):
+    def time_e2e(c, items, steps, graph=False):
         """Through the public call with host buffers: one pinned H2D copy of the
         step's inputs (x, ids and router weights packed in one staging buffer,
-        whose device twin the layer reads in place), the layer step (its
-        captured graph), D2H of y; all inside the timed region."""
+        whose device twin the layer reads in place), the layer step (the call,
+        or its captured graph), D2H of y; all inside the timed region, which
+        like the other timings opens on the stream right after the L2 flush
+        (the host has queued the step's work by then)."""
         T_max = max(it["T"] for it in items)
         layer = N.MoeLayer(W, T_max, c.k)
 
@@ -377,17 +379,20 @@ def gpu_bench(args, rank, world):
             dx, di, dw, _ = carve(dbuf, it)
             dbuf.copy_(hbuf)
             y = torch.empty_like(it["x"])
-            graphs.append(layer.capture(dx, di, dw, y))
-            dev_bufs.append(dict(buf=dbuf, y=y))
+            graphs.append(layer.capture(dx, di, dw, y) if graph else None)
+            dev_bufs.append(dict(buf=dbuf, y=y, x=dx, ids=di, tw=dw))
         ms, h2d, d2h, byts = [], [], [], []
         for i in range(steps + 3):
             h, d = host[i % len(host)], dev_bufs[i % len(host)]
-            flush_l2()
             torch.cuda.synchronize()
+            flush_l2()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             d["buf"].copy_(h["buf"], non_blocking=True)
-            graphs[i % len(host)].replay()
+            if graph:
+                graphs[i % len(host)].replay()
+            else:
+                layer(d["x"], d["ids"], d["tw"], d["y"])
             h["y"].copy_(d["y"], non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
@@ -425,7 +430,7 @@ def gpu_bench(args, rank, world):
     stages, gemm_bytes = time_stages(cfg, items, max(5, min(args.steps, 20)))
     peak, peak_kind = measured_peaks()
     achieved = gemm_bytes / (stages["expert_gemms"] * 1e-3) / 1e9
-    e2e_ms, e2e_bytes, h2d, d2h = time_e2e(cfg, items, max(5, min(args.steps, 20)))
+    e2e_ms, e2e_bytes, h2d, d2h = time_e2e(cfg, items, max(5, min(args.steps, 20)), graph=args.graph)
     e2e_gbs = world * sum(e2e_bytes) / (sum(e2e_ms) * 1e-3) / 1e9
 
     per_config = {}
