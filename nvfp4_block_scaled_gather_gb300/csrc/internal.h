@@ -41,14 +41,24 @@ int layer_arg_status(const uint16_t* x, int T, int H, int I, const int32_t* topk
                      const moe_nvfp4_weights_t* w, const uint16_t* y);
 
 // zero/nzero: an int array the route kernel also clears (may be null).
+// slot_sf (may be null): per slot s, the token block of bt rows (32 or 128)
+// and the row in it where slot s's row sits, as (block << 7) | row; -1 for
+// an unused slot.
 cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s,
-                         int* zero = nullptr, int nzero = 0);
+                         int* zero = nullptr, int nzero = 0, int* slot_sf = nullptr, int bt = 0);
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g,
                           uint16_t* xg, cudaStream_t s);
 // src_k > 0: rows are x[row_slot[r] / src_k]; src_k == 0: rows are src[r].
 // E bounds the group count (grid size); CTAs past the routed blocks exit.
 cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, int K,
                             const moe_groups_t& g, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
+// a2 + a3 token by token: each token row of x [T, K] quantized once and
+// written to each of its routed rows (packed [R_max, K/2], token scales in
+// `layout` at the places slot_sf gives, from launch_route with the matching
+// bt). The same bytes as launch_quantize(x, k, ...) for every routed row;
+// scale words of rows past a block's valid rows stay as they were.
+cudaError_t launch_quantize_tokens(const uint16_t* x, int T, int K, int k, const moe_groups_t& g,
+                                   const int* slot_sf, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s);
 // a1 + a2 + a3 in one launch for S = T*k <= 32 slots (rows x[slot / k]),
 // token scales in MOE_SF_CHUNK32; same outputs as launch_route followed by
 // launch_quantize(x, k, ...).

@@ -58,6 +58,7 @@ bool layout_ok(int layout) { return layout == MOE_SF_ATOM128 || layout == MOE_SF
 struct LayerWs {
   moe_groups_t groups;
   uint8_t *xq, *xsf, *hq, *hsf;
+  int* slot_sf;  // per slot, its place in the token-scale layout (batches of more than 32 slots)
   float* d2;
   int* gate;  // the GEMM's unit claim counter, finished CTAs, then w13 tiles finished per token block
   int ngate;
@@ -79,6 +80,7 @@ LayerWs carve_layer(void* base, int T, int k, int E, int H, int I) {
   uint8_t* gmem = take(moe_groups_bytes(T, k, E));
   if (base) moe_groups_carve(gmem, T, k, E, &w.groups);
   w.xq = take(S * H / 2);
+  w.slot_sf = S > (size_t)kSmallRouteSlots ? reinterpret_cast<int*>(take(S * sizeof(int))) : nullptr;
   const int layout = layer_sf_layout((long long)S, E);
   w.xsf = take(token_sf_bytes((long long)S, E, H, layout));
   w.hq = take(S * I / 2);
@@ -398,8 +400,11 @@ int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_
   if (small) {
     err = launch_route_quantize_small(topk_ids, S, E, ws.groups, ws.gate, ws.ngate, x, k, H, ws.xq, ws.xsf, stream);
   } else {
-    err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate);
-    if (err == cudaSuccess) err = launch_quantize(x, k, S, E, H, ws.groups, layout, ws.xq, ws.xsf, stream);
+    // each token row read and quantized once, written to all of its routed rows
+    err = launch_route(topk_ids, S, E, ws.groups, stream, ws.gate, ws.ngate, ws.slot_sf,
+                       layout == MOE_SF_ATOM128 ? 128 : 32);
+    if (err == cudaSuccess)
+      err = launch_quantize_tokens(x, T, H, k, ws.groups, ws.slot_sf, layout, ws.xq, ws.xsf, stream);
   }
   const SmallFront front{topk_ids, S};
   // a4 + a5 + a6 (w13 with SwiGLU and requantization in its epilogue) and a7

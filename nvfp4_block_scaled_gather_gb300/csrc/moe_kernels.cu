@@ -32,13 +32,15 @@ constexpr int kThreads = 256;
 // Rows therefore ascend by (expert, slot), a pure function of the routing.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__ ids, int S, int E,
-                                                     moe_groups_t g, int* __restrict__ zero, int nzero) {
+                                                     moe_groups_t g, int* __restrict__ zero, int nzero,
+                                                     int* __restrict__ slot_sf, int bt) {
   pdl_wait();  // the previous kernel in the stream may still be running
   pdl_trigger();
   for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   extern __shared__ int32_t smem[];
   int32_t* wc = smem;                // [32][E]: counts, then running row cursors
   int32_t* rowbase = smem + 32 * E;  // [E]: first row of each expert
+  int32_t* blkbase = smem + 33 * E;  // [E]: its first token block of bt rows (slot_sf only)
   __shared__ int32_t wsum[32][4];
   __shared__ int32_t wmax[32];
   __shared__ int32_t tot[5];
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
     const int blk0 = v2 - own2 + wsum[w][2];
     const int chk0 = v3 - own3 + wsum[w][3];
     rowbase[tid] = row0;
+    if (slot_sf) blkbase[tid] = bt == 128 ? blk0 : chk0;
     if (cnt > 0) {
       g.group_expert[gi] = tid;
       g.group_offsets[gi] = row0;
@@ -132,11 +135,14 @@ __global__ void __launch_bounds__(1024) route_kernel(const int32_t* __restrict__
     int cur = 0;
     if (ok) {
       cur = wc[w * E + e];
-      const int row = rowbase[e] + cur + rank;
+      const int local = cur + rank;  // the row's place in its expert's group
+      const int row = rowbase[e] + local;
       g.row_slot[row] = s;
       g.slot_row[s] = row;
+      if (slot_sf) slot_sf[s] = ((blkbase[e] + local / bt) << 7) | (local % bt);
     } else if (in) {
       g.slot_row[s] = -1;
+      if (slot_sf) slot_sf[s] = -1;
     }
     __syncwarp();
     if (ok && rank == n - 1) wc[w * E + e] = cur + n;
@@ -305,6 +311,58 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
     }
   }
   st.zero_rest(kc0 / 64, kcount / 64, rb.nvalid);
+}
+
+// ---------------------------------------------------------------------------
+// a2 + a3 token by token (the layer's path for more than 32 slots): each
+// token row of x is read and quantized once, and its codes and block scales
+// are written to every routed row of the token (slot_row) and the row's
+// place in the token-scale layout (slot_sf); the same bytes as
+// quantize_kernel for every routed row. Scale words of rows past a block's
+// valid rows are not written: they feed only accumulator columns no result
+// reads. Grid: (8 tokens, 512-value column chunk); warp w takes token
+// 8 blockIdx.x + w, lane l its 16-value block l.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) quantize_tokens_kernel(const uint16_t* __restrict__ x, int T, int K,
+                                                                   int k, moe_groups_t g,
+                                                                   const int* __restrict__ slot_sf, int layout,
+                                                                   uint8_t* __restrict__ packed,
+                                                                   uint8_t* __restrict__ sf) {
+  pdl_wait();  // the tables come from the previous kernel
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int Kc = K / 16;
+  const int kc0 = blockIdx.y * kQuantCols;
+  const int kcount = min(kQuantCols, K - kc0);  // a multiple of 64
+  const bool lane_on = 16 * lane < kcount;
+  // the token's routed rows and scale places, lane j holding slot j's, in flight with the row
+  const int row = lane < k ? ld_cg(g.slot_row + (size_t)t * k + lane) : -1;
+  const int pos = lane < k ? ld_cg(slot_sf + (size_t)t * k + lane) : -1;
+  uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+  if (lane_on) {
+    const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)t * K + kc0 + 16 * lane);
+    u0 = ld_cg(p);
+    u1 = ld_cg(p + 1);
+  }
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  uint2 codes;
+  uint32_t scale;
+  quantize_block16(v, codes, scale);
+  for (int j = 0; j < k; ++j) {
+    const int r = __shfl_sync(~0u, row, j), q = __shfl_sync(~0u, pos, j);
+    if (r < 0 || !lane_on) continue;  // an unused slot (the same in every lane)
+    *reinterpret_cast<uint2*>(packed + (size_t)r * (K / 2) + kc0 / 2 + 8 * lane) = codes;
+    const ScaleTarget st{sf + (size_t)(q >> 7) * 128 * Kc, layout, Kc};
+    *st.byte(q & 127, kc0 / 16 + lane) = (uint8_t)scale;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -620,13 +678,15 @@ int grid_for(long long items) {
 }  // namespace
 
 cudaError_t launch_route(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, cudaStream_t s, int* zero,
-                         int nzero) {
-  const size_t smem = (size_t)33 * E * sizeof(int32_t);
+                         int nzero, int* slot_sf, int bt) {
+  if (slot_sf && bt != 32 && bt != 128) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)34 * E * sizeof(int32_t);
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  return launch_pdl(route_kernel, dim3(1), dim3(1024), smem, s, topk_ids, S, E, g, zero, zero ? nzero : 0);
+  return launch_pdl(route_kernel, dim3(1), dim3(1024), smem, s, topk_ids, S, E, g, zero, zero ? nzero : 0, slot_sf,
+                    bt > 0 ? bt : 32);
 }
 
 cudaError_t launch_gather(const uint16_t* x, int H, int k, int R_max, const moe_groups_t& g, uint16_t* xg,
@@ -638,6 +698,14 @@ cudaError_t launch_quantize(const uint16_t* src, int src_k, int R_max, int E, in
                             int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
   const dim3 grid((unsigned)row_blocks_bound(R_max, E, layout), (K + kQuantCols - 1) / kQuantCols);
   return launch_pdl(quantize_kernel, grid, dim3(kThreads), 0, s, src, src_k, K, g, layout, packed, sf);
+}
+
+cudaError_t launch_quantize_tokens(const uint16_t* x, int T, int K, int k, const moe_groups_t& g,
+                                   const int* slot_sf, int layout, uint8_t* packed, uint8_t* sf, cudaStream_t s) {
+  if (K % 64 || k < 1 || k > kMaxTopK || (layout != MOE_SF_ATOM128 && layout != MOE_SF_CHUNK32))
+    return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((T + kThreads / 32 - 1) / (kThreads / 32)), (K + kQuantCols - 1) / kQuantCols);
+  return launch_pdl(quantize_tokens_kernel, grid, dim3(kThreads), 0, s, x, T, K, k, g, slot_sf, layout, packed, sf);
 }
 
 cudaError_t launch_route_quantize_small(const int32_t* topk_ids, int S, int E, const moe_groups_t& g, int* zero,
