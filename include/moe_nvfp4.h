@@ -303,9 +303,12 @@ int moe_nvfp4_layer_sf_layout(int T, int k, int E);
  * (T*k <= 32: route + gather + quantize in one). Each launch may start while
  * the previous one finishes (programmatic dependent launch). Token rows go
  * through the GEMMs in blocks of moe_nvfp4_layer_sf_layout(T, k, E).
- * x [T, H] bf16, y [T, H] bf16 (overwritten). `workspace` is caller device
- * memory of ws_bytes >= moe_nvfp4_layer_workspace_size(T, k, w->E, H, I),
- * 256-byte aligned (any contents). Calls sharing a workspace run in stream
+ * x [T, H] bf16, y [T, H] bf16 (overwritten). With k > 0, x, topk_ids,
+ * topk_w and y may also be pinned host memory (unified addressing): the
+ * kernels then read and write them in place over the CPU-GPU link.
+ * `workspace` is caller device memory of ws_bytes >=
+ * moe_nvfp4_layer_workspace_size(T, k, w->E, H, I), 256-byte aligned (any
+ * contents). Calls sharing a workspace run in stream
  * order. H % 128 == 0, I % 128 == 0, k <= 32, E <= 1024. */
 int moe_nvfp4_layer(const uint16_t* x, int T, int H, int I, const int32_t* topk_ids,
                     const float* topk_w, int k, const moe_nvfp4_weights_t* w /* host struct */,

@@ -551,3 +551,23 @@ def test_full_size_layer(cuda, full_weights, name, tokens):
     for t in tokens:
         _token_check(t, x_np, ids_np, tw_np, w_or, cfg.E, y, st)
     assert N.check_status() == 0
+
+
+@pytest.mark.parametrize("n", [1, 3, 40, 60])
+def test_layer_reads_and_writes_pinned_host_buffers(small, n):
+    """x, the routing, the router weights and y may sit in pinned host memory
+    (unified addressing: the kernels read and write them over the CPU-GPU
+    link): the same bits as the call on device buffers, for the one-launch
+    decode front end (n = 1, 3) and the general path with 32-row (40) and
+    128-row (60) token blocks."""
+    E, x, ids, tw, W, *_ = small
+    k = ids.shape[1]
+    xd, idd, twd = x[:n].contiguous(), ids[:n].contiguous(), tw[:n].contiguous()
+    layer = N.MoeLayer(W, n, k)
+    want = layer(xd, idd, twd).clone()
+    hx, hi, hw = xd.cpu().pin_memory(), idd.cpu().pin_memory(), twd.cpu().pin_memory()
+    hy = torch.full_like(hx, 7.0).pin_memory()
+    layer(hx, hi, hw, hy)
+    torch.cuda.synchronize()
+    assert torch.equal(hy.view(torch.int16), want.cpu().view(torch.int16))
+    assert N.check_status() == 0
