@@ -571,3 +571,27 @@ def test_layer_reads_and_writes_pinned_host_buffers(small, n):
     torch.cuda.synchronize()
     assert torch.equal(hy.view(torch.int16), want.cpu().view(torch.int16))
     assert N.check_status() == 0
+
+
+@pytest.mark.parametrize("n", [3, 40, 60])
+def test_layer_ignores_workspace_contents(small, n):
+    """The workspace may hold anything (the header's "any contents"): filled
+    with 0xFF bytes first (NaN e4m3 scale codes, NaN-pattern codes and
+    counters far past their ends), every call gives the bits of a call on a
+    zeroed workspace; the token-scale padding a step never writes only feeds
+    accumulator columns no result reads."""
+    E, x, ids, tw, W, *_ = small
+    k = ids.shape[1]
+    c = (x[:n].contiguous(), ids[:n].contiguous(), tw[:n].contiguous())
+    size = N.moe_nvfp4_layer_workspace_size(n, k, E, W.H, W.I)
+    ws0 = torch.zeros(size, dtype=torch.uint8, device=x.device)
+    want = torch.empty_like(c[0])
+    N.moe_nvfp4_layer(*c, W, ws0, want)
+    ws = torch.full((size,), 0xFF, dtype=torch.uint8, device=x.device)
+    for _ in range(2):
+        y = torch.empty_like(c[0])
+        N.moe_nvfp4_layer(*c, W, ws, y)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), want.view(torch.int16))
+        ws.fill_(0xFF)
+    assert N.check_status() == 0
