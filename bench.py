@@ -309,8 +309,11 @@ def gpu_bench(args, rank, world):
         return ms, byts
 
     def time_stages(c, items, steps):
-        """Same kernels as the fused entry, launched stage by stage with
-        events between them (per-kernel device time)."""
+        """The step through the separate entry points, stage by stage with
+        events between them: route, gather + quantize by rows, the two-GEMM
+        launch (the layer's own GEMM kernel and token blocks), scatter. The
+        layer itself routes and quantizes in one launch for decode batches and
+        quantizes token by token otherwise."""
         T_max = max(it["T"] for it in items)
         S = T_max * c.k
         lay = N.layer_sf_layout(T_max, c.k, c.E)  # the token blocks the layer itself takes
