@@ -595,3 +595,28 @@ def test_layer_ignores_workspace_contents(small, n):
         assert torch.equal(y.view(torch.int16), want.view(torch.int16))
         ws.fill_(0xFF)
     assert N.check_status() == 0
+
+
+@pytest.mark.parametrize("E,H,I,T,k,seed", [(3, 256, 128, 1, 1, 0), (8, 384, 256, 5, 2, 1), (5, 640, 384, 17, 4, 2),
+                                            (16, 256, 384, 40, 3, 3), (4, 512, 128, 70, 1, 4),
+                                            (12, 384, 640, 9, 8, 5)])
+def test_layer_over_shapes(cuda, E, H, I, T, k, seed):
+    """The layer over a spread of shapes (K tails in both GEMMs, 1 to 12
+    token blocks per expert, decode and general paths, top-1 to top-8):
+    the separate entry points' bits and within 1e-2 of the oracle."""
+    from nvfp4_block_scaled_gather_gb300.synthetic import make_weights as mw
+    g = torch.Generator().manual_seed(1000 + seed)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    ids[torch.rand((T, k), generator=g) < 0.1] = -1                   # some unused slots
+    tw = torch.rand((T, k), generator=g)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    w = mw(E, H, I, seed=seed)
+    w_np = {kk: v.numpy() for kk, v in w.items()}
+    W = weights_from({kk: v.to(cuda) for kk, v in w.items()})
+    xd, idd, twd = x.to(cuda), ids.to(cuda), tw.to(cuda)
+    y = N.MoeLayer(W, T, k)(xd, idd, twd)
+    st = run_stages(xd, idd, twd, W, E)
+    assert torch.equal(y.view(torch.int16), st["y"].view(torch.int16))
+    ref = O.moe_layer(bf16_to_np(x), ids.numpy(), tw.numpy(), w_np, E=E)
+    assert rel_fro(O.bf16_bits_to_f64(bf16_to_np(y)), O.bf16_bits_to_f64(ref["y"])) <= LAYER_TOL
+    assert N.check_status() == 0
